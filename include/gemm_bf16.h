@@ -1,0 +1,196 @@
+/*
+ * gemm_bf16.h -- C ABI of a persistent, warp-specialised, TMA-fed bf16 GEMM for
+ * NVIDIA GB300 (sm_103a):
+ *
+ *     D[m][n] = bf16( sum_k A[m][k] * B[n][k] ),  0 <= m < M, 0 <= n < N
+ *
+ * A is M x K and B is N x K, both row-major with the contraction index
+ * contiguous ("K-major"), bf16; products are accumulated in fp32 in tensor
+ * memory and rounded once to bf16 (nearest, ties to even) when stored.
+ *
+ * Where the operation and its pipeline come from:
+ *  - Fuser issue #3941, "Allow separate sub-DAG for load and compute warp groups
+ *    with warp-specialized circular buffering": the persistent matmul (a
+ *    grid-stride loop over output tiles with a cta-k loop inside), the load warp
+ *    group's merged tile x cta-k loop, the compute side's separate tile and k
+ *    loops, the fp32 -> bf16 epilogue with a TMA store, and the register
+ *    rebalancing between load and compute warps (Scheduling Proposal,
+ *    Lowering Proposal, Pseudo-code).
+ *  - Fuser PR #3446, "Use mbarrier for WAR for circular buffering": the stage
+ *    ring with one "full" barrier (data landed, read-after-write) and one
+ *    "empty" barrier (data fully read, write-after-read) per stage, and the
+ *    __syncthreads-WAR loop it replaces (both kept as ablations).
+ *  - cutlass PR #3316, "[Tutorial] Fix race condition in 2SM TMEM alloc for Cute
+ *    Blackwell Tutorial 04/05": in the 2-CTA (paired-SM) mode a cluster barrier
+ *    precedes the paired tensor-memory allocation.
+ *
+ * Conventions for every entry point:
+ *  - Return value: GEMM_BF16_OK (0) or a negative gemm_bf16_status.  No entry
+ *    point aborts, throws or prints; gemm_bf16_strerror() names a status.
+ *  - Device pointers are plain CUDA device addresses of the device the handle
+ *    was created on; the caller owns them.  "stream" is a cudaStream_t passed as
+ *    void* (NULL = the legacy default stream); the caller owns it.
+ *  - A handle is not thread-safe: use one handle per host thread.
+ */
+#ifndef GEMM_BF16_H
+#define GEMM_BF16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define GEMM_BF16_API __declspec(dllexport)
+#else
+#define GEMM_BF16_API __attribute__((visibility("default")))
+#endif
+
+typedef struct gemm_bf16 *gemm_bf16_t;
+
+typedef enum gemm_bf16_status {
+    GEMM_BF16_OK = 0,
+    GEMM_BF16_ERR_INVALID_ARG = -1,    /* null handle/pointer, size <= 0, ld < extent, bad option */
+    GEMM_BF16_ERR_ALIGNMENT = -2,      /* a TMA rule broken: A/B base not 16-byte aligned, lda*2 or ldb*2 not a multiple of 16 */
+    GEMM_BF16_ERR_NOT_PLANNED = -3,    /* run before a successful plan */
+    GEMM_BF16_ERR_CUDA = -4,           /* a CUDA runtime call failed (launch, copy, allocation) */
+    GEMM_BF16_ERR_TENSORMAP = -5,      /* the driver refused a TMA tensor-map encoding */
+    GEMM_BF16_ERR_DEVICE_TIMEOUT = -6, /* a kernel's bounded barrier wait ran out; the kernel returned early */
+    GEMM_BF16_ERR_UNSUPPORTED = -7     /* device is not sm_103, or the option combination cannot run on it */
+} gemm_bf16_status;
+
+/* Pipeline variants (GEMM_BF16_OPT_PIPELINE). */
+typedef enum gemm_bf16_pipeline {
+    /* Warp-specialised: one TMA producer warp, one tcgen05 MMA warp, two epilogue
+     * warpgroups; full/empty mbarrier ring; persistent tile loop. (default) */
+    GEMM_BF16_PIPE_WS = 0,
+    /* Not specialised, write-after-read guarded by __syncthreads(): one elected
+     * thread loads and issues the MMAs; every thread waits for the data and for
+     * the MMAs to finish, then the block synchronises (the loop Fuser PR #3446
+     * starts from).  One tile per CTA, 1-CTA mode only. */
+    GEMM_BF16_PIPE_SYNC_WAR = 1,
+    /* Not specialised, write-after-read guarded by an "empty" mbarrier per stage
+     * that the MMA completion arrives on (the loop Fuser PR #3446 adds).  One
+     * tile per CTA, 1-CTA mode only. */
+    GEMM_BF16_PIPE_MBAR_WAR = 2
+} gemm_bf16_pipeline;
+
+/* Options, set before gemm_bf16_plan (a later plan picks them up). */
+typedef enum gemm_bf16_option {
+    GEMM_BF16_OPT_PIPELINE = 1,      /* gemm_bf16_pipeline; default GEMM_BF16_PIPE_WS */
+    GEMM_BF16_OPT_CTA_GROUP = 2,     /* 0 = automatic (default), 1 = one SM per tile (128x256),
+                                        2 = SM pair per tile (256x256, cta_group::2, WS only) */
+    GEMM_BF16_OPT_PERSISTENT = 3,    /* 1 (default): grid = resident CTAs, grid-stride tile loop;
+                                        0: one tile per CTA (grid = tiles) */
+    GEMM_BF16_OPT_ACC_BUFFERS = 4,   /* tensor-memory accumulators per CTA: 2 (default) lets the
+                                        epilogue of a tile overlap the next tile's main loop; 1 */
+    GEMM_BF16_OPT_SETMAXNREG = 5,    /* 1 (default): the producer/MMA warpgroup drops to 56
+                                        registers per thread and the epilogue warpgroups rise
+                                        to 224; 0: no rebalancing */
+    GEMM_BF16_OPT_STAGES = 6,        /* stage-ring depth; 0 (default) = as deep as shared memory allows */
+    GEMM_BF16_OPT_RASTER_GROUP = 7,  /* tile order: groups of this many tile rows walked column by
+                                        column (default 8); 0 = plain row-major */
+    GEMM_BF16_OPT_EPILOGUE = 8,      /* 0 = automatic (default): TMA store when D's base is 16-byte
+                                        aligned and ldd*2 is a multiple of 16, else masked stores;
+                                        1 = TMA store (run fails with ALIGNMENT if not allowed);
+                                        2 = masked coalesced st.global */
+    GEMM_BF16_OPT_MAX_CTAS = 9,      /* upper bound on the persistent grid (0 = no bound) */
+    GEMM_BF16_OPT_WATCHDOG_NS = 10,  /* limit of every in-kernel barrier wait, ns (default 1e9) */
+    GEMM_BF16_OPT_FAULT_SKIP_LOAD = 11 /* test hook: each CTA's producer skips its load at this
+                                          ring iteration, so the MMA warp's wait runs out and
+                                          the kernel reports GEMM_BF16_ERR_DEVICE_TIMEOUT;
+                                          -1 (default) = off */
+} gemm_bf16_option;
+
+/* What a plan resolved to (filled by gemm_bf16_plan_info). */
+typedef struct gemm_bf16_plan_info_s {
+    int64_t tiles;                /* output tiles (one per CTA pair in 2-CTA mode) */
+    int64_t k_blocks;             /* 64-wide k-blocks per tile */
+    int32_t grid_ctas;            /* CTAs per launch */
+    int32_t threads_per_cta;
+    int32_t cta_group;            /* 1 or 2 */
+    int32_t pipeline;             /* gemm_bf16_pipeline */
+    int32_t persistent;
+    int32_t stages;               /* stage-ring depth */
+    int32_t acc_buffers;
+    int32_t setmaxnreg;
+    int32_t tile_m;               /* rows of D per tile */
+    int32_t tile_n;               /* columns of D per tile */
+    int32_t tile_k;               /* k per stage */
+    int32_t smem_bytes;           /* dynamic shared memory per CTA */
+    int32_t num_sms;
+    int32_t epilogue_tma_allowed; /* 1 if ldd permits the TMA-store epilogue */
+    int32_t raster_group;
+    int32_t regs_per_thread;      /* registers per thread the kernel is launched with */
+} gemm_bf16_plan_info_t;
+
+/* Creates a handle bound to CUDA device `device` (-1 = the calling thread's
+ * current device).  Allocates the handle (host) and a 4-byte device status word
+ * that the kernels' watchdog writes.  Fails with UNSUPPORTED unless the device
+ * is compute capability 10.3 (sm_103), with CUDA if no device is usable.
+ * On success *out owns both allocations until gemm_bf16_destroy. */
+GEMM_BF16_API int gemm_bf16_create(int device, gemm_bf16_t *out);
+
+/* Frees the handle.  Waits for nothing: the caller must not destroy a handle
+ * whose launches are still running.  NULL is accepted (no-op). */
+GEMM_BF16_API int gemm_bf16_destroy(gemm_bf16_t h);
+
+/* Sets one option (gemm_bf16_option) for the next gemm_bf16_plan.
+ * INVALID_ARG for an unknown key or a value outside the documented range. */
+GEMM_BF16_API int gemm_bf16_set_option(gemm_bf16_t h, int key, int64_t value);
+GEMM_BF16_API int gemm_bf16_get_option(gemm_bf16_t h, int key, int64_t *value);
+
+/* Host-only validation of a problem shape, shared by gemm_bf16_plan and usable
+ * without a GPU.  INVALID_ARG: M, N or K < 1 or > 2^31-1, lda < K, ldb < K or
+ * ldd < N.  ALIGNMENT: lda*2 or ldb*2 not a multiple of 16 bytes (every row of
+ * a TMA-loaded operand must start 16-byte aligned).  ldd may be any value >= N. */
+GEMM_BF16_API int gemm_bf16_check_problem(int64_t M, int64_t N, int64_t K,
+                                          int64_t lda, int64_t ldb, int64_t ldd);
+
+/* Validates the problem (as gemm_bf16_check_problem), resolves the options,
+ * and picks the kernel, stage count, tile order and grid.  Re-planning a handle
+ * is allowed and replaces the previous plan.  Launches nothing. */
+GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
+                                 int64_t lda, int64_t ldb, int64_t ldd);
+
+/* Fills *info from the current plan (NOT_PLANNED before one). */
+GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info);
+
+/* Enqueues D = A * B^T on `stream` and returns without synchronising.
+ *   A: device, M rows of lda bf16 (first K read);  B: device, N rows of ldb;
+ *   D: device, M rows of ldd bf16 -- only the M x N sub-matrix is written.
+ * A and B must be 16-byte aligned (ALIGNMENT otherwise), D 2-byte aligned.
+ * The TMA tensor maps are rebuilt only when a pointer differs from the last run.
+ * Argument errors are returned before anything is enqueued; a launch failure
+ * returns CUDA.  A watchdog timeout inside the kernel is reported later by
+ * gemm_bf16_device_status. */
+GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, void *D,
+                                void *stream);
+
+/* End-to-end variant with HOST operands: enqueues on `stream` the copies
+ * hA -> dA and hB -> dB (the M x K and N x K sub-matrices, row pitches lda and
+ * ldb), the GEMM on dA, dB, dD, and the copy of the M x N result dD -> hD (row
+ * pitch ldd).  Returns without synchronising; page-locked host buffers make the
+ * copies asynchronous.  The caller owns all six buffers. */
+GEMM_BF16_API int gemm_bf16_run_host(gemm_bf16_t h, const void *hA, const void *hB, void *hD,
+                                     void *dA, void *dB, void *dD, void *stream);
+
+/* Synchronises the stream of the last run, reads and clears the device status
+ * word.  Returns OK, or DEVICE_TIMEOUT if a kernel's bounded wait ran out since
+ * the last call (then *detail, if not NULL, receives the recorded word: bit 31
+ * set, bits 24..27 the waiting role, bits 12..23 the CTA, bits 0..11 the ring
+ * stage or buffer). */
+GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail);
+
+/* Static, never-NULL description of a status code. */
+GEMM_BF16_API const char *gemm_bf16_strerror(int status);
+
+/* Library version string, e.g. "gemm_bf16 1.0 sm_103a". */
+GEMM_BF16_API const char *gemm_bf16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_BF16_H */

@@ -1,0 +1,286 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Tolerance (per element, against the oracle's unrounded fp64 sum ref64):
+    |d - ref64| <= 4e-3 * |ref64| + 2e-3 * sqrt(K) * sigma_A * sigma_B
+with sigma the RMS of the generated operand.  Integer-valued inputs make every
+fp32 partial sum exact, so there the bf16 result must equal the oracle's bf16
+rounding bit for bit.  Padding columns of D (n >= N) must never be written.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from warp_specialized_tma_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL_BITS = 0x7FC1  # a NaN pattern no correct kernel writes
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from warp_specialized_tma_gb300 import build as libbuild
+    libbuild.build()
+    binding.load()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def rms(t: torch.Tensor, K: int) -> float:
+    v = t[:, :K].double()
+    return float(v.pow(2).mean().sqrt())
+
+
+def run_gpu(A, B, M, N, K, ldd=None, **opts):
+    """D (CPU, M x ldd bf16) computed on the GPU through the C ABI."""
+    ldd = N if ldd is None else ldd
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.full((M, ldd), 0, dtype=torch.int16, device=dev)
+    dD.fill_(SENTINEL_BITS - 0x10000 if SENTINEL_BITS > 0x7FFF else SENTINEL_BITS)
+    dD = dD.view(torch.bfloat16)
+    with binding.Gemm(0, **opts) as g:
+        g.plan(M, N, K, A.shape[1], B.shape[1], ldd)
+        g.run(dA, dB, dD)
+        st, detail = g.device_status()
+        assert st == binding.OK, f"device status {st} detail {detail:#x}"
+    torch.cuda.synchronize()
+    return dD.cpu()
+
+
+def check(D, A, B, M, N, K, rows=None, exact=False):
+    """Compares rows of D with the oracle; returns the max abs error."""
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    ref64, refbf = oracle.gemm_rows(inputs.bits(A), inputs.bits(B), K=K, rows=rows)
+    Dbits = inputs.bits(D)
+    got_bits = Dbits[rows][:, :N]
+    if exact:
+        bad = np.argwhere(got_bits != refbf)
+        assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+    got = inputs.from_bits(np.ascontiguousarray(got_bits)).double().numpy()
+    tol = 4e-3 * np.abs(ref64) + 2e-3 * math.sqrt(K) * rms(A, K) * rms(B, K)
+    err = np.abs(got - ref64)
+    bad = np.argwhere(~(err <= tol))
+    assert bad.size == 0, (f"{len(bad)} elements outside tolerance, first {bad[:5].tolist()}, "
+                           f"max err {np.nanmax(err):.4g}")
+    # columns beyond N keep the sentinel
+    if Dbits.shape[1] > N:
+        assert np.all(Dbits[:, N:] == SENTINEL_BITS)
+    return float(np.max(err)) if err.size else 0.0
+
+
+def sample_rows(M: int, tile_m: int = 128, seed: int = 0, extra: int = 16):
+    """First/last row of every 128-row slab plus random rows."""
+    rng = np.random.default_rng(seed)
+    rows = set()
+    for s in range(0, M, tile_m):
+        rows.add(s)
+        rows.add(min(M - 1, s + tile_m - 1))
+        rows.add(min(M - 1, s + 31 + (s // tile_m) % 64))
+    rows.update(rng.integers(0, M, size=extra).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+# ------------------------------------------------------------------ small shapes
+TINY = [(1, 1, 1), (1, 1, 8), (2, 3, 5), (5, 8, 7), (8, 8, 8), (3, 1, 4), (7, 5, 2)]
+
+
+@pytest.mark.parametrize("M,N,K", TINY)
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_tiny_shapes(M, N, K, cta_group):
+    A, B = inputs.make_problem(M, N, K, "normal", seed=M * 100 + N * 10 + K, lda=8, ldb=8)
+    D = run_gpu(A, B, M, N, K, ldd=N, cta_group=cta_group)
+    check(D, A, B, M, N, K)
+    Ai, Bi = inputs.make_problem(M, N, K, "int2", seed=K, lda=8, ldb=8)
+    check(run_gpu(Ai, Bi, M, N, K, cta_group=cta_group), Ai, Bi, M, N, K, exact=True)
+
+
+MID = [(256, 256, 256), (300, 520, 200), (129, 257, 65), (640, 384, 1000), (1000, 1000, 1000)]
+
+
+@pytest.mark.parametrize("M,N,K", MID)
+@pytest.mark.parametrize("variant", [
+    dict(cta_group=1),
+    dict(cta_group=2),
+    dict(cta_group=1, setmaxnreg=0),
+    dict(cta_group=2, setmaxnreg=0),
+    dict(cta_group=2, acc_buffers=1),
+    dict(cta_group=1, persistent=0),
+    dict(cta_group=2, persistent=0),
+    dict(pipeline=binding.PIPE_SYNC_WAR),
+    dict(pipeline=binding.PIPE_MBAR_WAR),
+])
+def test_mid_shapes_all_variants(M, N, K, variant):
+    A, B = inputs.make_problem(M, N, K, "normal", seed=M + N + K)
+    check(run_gpu(A, B, M, N, K, **variant), A, B, M, N, K)
+    Ai, Bi = inputs.make_problem(M, N, K, "int2", seed=M + N + K + 1)
+    check(run_gpu(Ai, Bi, M, N, K, **variant), Ai, Bi, M, N, K, exact=True)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("max_ctas,stages", [(2, 2), (4, 3), (6, 0)])
+def test_few_ctas_many_tiles_ring_wraps(cta_group, max_ctas, stages):
+    # few persistent CTAs walk many tiles: the ring and the accumulator
+    # barriers wrap across tile boundaries many times
+    M, N, K = 1100, 1300, 520
+    A, B = inputs.make_problem(M, N, K, "int2", seed=21)
+    D = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stages=stages)
+    check(D, A, B, M, N, K, exact=True)
+
+
+@pytest.mark.parametrize("epilogue,ldd", [(0, 520), (1, 520), (2, 520), (0, 523), (2, 528)])
+def test_epilogue_paths_and_padding(epilogue, ldd):
+    M, N, K = 333, 517, 96
+    A, B = inputs.make_problem(M, N, K, "normal", seed=5)
+    D = run_gpu(A, B, M, N, K, ldd=ldd, epilogue=epilogue)
+    check(D, A, B, M, N, K)
+
+
+@pytest.mark.parametrize("raster_group", [0, 1, 3, 8, 64])
+def test_raster_orders(raster_group):
+    M, N, K = 1536, 1280, 128
+    A, B = inputs.make_problem(M, N, K, "int2", seed=3)
+    check(run_gpu(A, B, M, N, K, raster_group=raster_group, max_ctas=10), A, B, M, N, K, exact=True)
+
+
+def test_identity_and_permutation_full_tiles():
+    # B = I gives D = A bit for bit; A = P gives D[m, n] = B[n, perm[m]]
+    K = 1024
+    g = torch.Generator().manual_seed(9)
+    A = inputs.make_operand(768, K, None, "normal", g)
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    D = run_gpu(A, eye, 768, K, K)
+    assert torch.equal(D.view(torch.int16), A.view(torch.int16))
+    perm = torch.randperm(K, generator=g)
+    P = torch.zeros((K, K), dtype=torch.bfloat16)
+    P[torch.arange(K), perm] = 1.0
+    Bm = inputs.make_operand(640, K, None, "uniform", g)
+    D2 = run_gpu(P, Bm, K, 640, K)
+    assert torch.equal(D2.view(torch.int16), Bm[:, perm].t().contiguous().view(torch.int16))
+
+
+# ------------------------------------------------------------------ the five workloads
+@pytest.mark.parametrize("name", list(inputs.WORKLOADS))
+def test_workload_sampled_rows(name):
+    w = inputs.WORKLOADS[name]
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.make_workload(name)
+    D = run_gpu(A, B, M, N, K)
+    rows = sample_rows(M) if M > 512 else None
+    check(D, A, B, M, N, K, rows=rows)
+
+
+@pytest.mark.parametrize("name", list(inputs.WORKLOADS))
+def test_workload_integer_inputs_exact(name):
+    w = inputs.WORKLOADS[name]
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.make_problem(M, N, K, "int2", seed=w["seed"] + 100)
+    D = run_gpu(A, B, M, N, K)
+    rows = sample_rows(M, seed=1, extra=8) if M > 512 else None
+    check(D, A, B, M, N, K, rows=rows, exact=True)
+
+
+def test_ragged_padded_ldd_uses_tma_store():
+    w = inputs.WORKLOADS["ragged"]
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.make_workload("ragged")
+    D = run_gpu(A, B, M, N, K, ldd=6000, epilogue=1)
+    check(D, A, B, M, N, K, rows=sample_rows(M, seed=2, extra=8))
+
+
+def test_all_ones_full_size_property():
+    # every entry of D is exactly K (K <= 256 keeps it representable in bf16)
+    M, N, K = 4096, 4096, 256
+    A = torch.ones((M, K), dtype=torch.bfloat16)
+    D = run_gpu(A, A, M, N, K)
+    assert torch.all(D.float() == K)
+
+
+# ------------------------------------------------------------------ boundary behaviour
+def test_run_before_plan_and_bad_pointers():
+    dev = torch.device("cuda:0")
+    buf = torch.zeros(4096, dtype=torch.bfloat16, device=dev)
+    st, h = binding.gemm_bf16_create(0)
+    assert st == binding.OK
+    try:
+        p = buf.data_ptr()
+        assert binding.gemm_bf16_run(h, p, p, p) == binding.ERR_NOT_PLANNED
+        assert binding.gemm_bf16_plan(h, 16, 16, 16, 16, 16, 16) == binding.OK
+        assert binding.gemm_bf16_run(h, p + 2, p, p) == binding.ERR_ALIGNMENT
+        assert binding.gemm_bf16_run(h, p, p + 8, p) == binding.ERR_ALIGNMENT
+        assert binding.gemm_bf16_run(h, p, p, p + 1) == binding.ERR_ALIGNMENT
+        assert binding.gemm_bf16_run(h, 0, p, p) == binding.ERR_INVALID_ARG
+        assert binding.gemm_bf16_set_option(h, 99, 0) == binding.ERR_INVALID_ARG
+        assert binding.gemm_bf16_set_option(h, binding.OPTIONS["stages"], 99) == binding.ERR_INVALID_ARG
+        # forcing the TMA-store epilogue on an odd ldd is refused before launch
+        assert binding.gemm_bf16_set_option(h, binding.OPTIONS["epilogue"], 1) == binding.OK
+        assert binding.gemm_bf16_plan(h, 16, 15, 16, 16, 16, 15) == binding.OK
+        assert binding.gemm_bf16_run(h, p, p, p) == binding.ERR_ALIGNMENT
+        # the ablation loops are single-CTA only
+        assert binding.gemm_bf16_set_option(h, binding.OPTIONS["pipeline"], binding.PIPE_SYNC_WAR) == binding.OK
+        assert binding.gemm_bf16_set_option(h, binding.OPTIONS["cta_group"], 2) == binding.OK
+        assert binding.gemm_bf16_plan(h, 16, 16, 16, 16, 16, 16) == binding.ERR_UNSUPPORTED
+    finally:
+        torch.cuda.synchronize()
+        binding.gemm_bf16_destroy(h)
+
+
+def test_plan_info_reports_the_configuration():
+    with binding.Gemm(0) as g:
+        info = g.plan(8192, 8192, 8192)
+        assert info["cta_group"] == 2 and info["tile_m"] == 256 and info["tile_n"] == 256
+        assert info["tiles"] == 32 * 32 and info["k_blocks"] == 128
+        assert info["grid_ctas"] % 2 == 0 and info["grid_ctas"] <= info["num_sms"]
+        assert info["stages"] >= 4 and info["acc_buffers"] == 2
+        assert info["regs_per_thread"] * info["threads_per_cta"] <= 65536
+
+
+@pytest.mark.parametrize("variant", [dict(cta_group=1), dict(cta_group=2),
+                                     dict(pipeline=binding.PIPE_MBAR_WAR)])
+def test_watchdog_reports_timeout_and_context_survives(variant):
+    # the producer skips one load: the MMA warp's bounded wait runs out, the
+    # kernel returns early with a status word instead of hanging
+    M, N, K = 512, 512, 1024
+    A, B = inputs.make_problem(M, N, K, "normal", seed=2)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0, watchdog_ns=20_000_000, fault_skip_load=3, **variant) as g:
+        g.plan(M, N, K)
+        g.run(dA, dB, dD)
+        st, detail = g.device_status()
+        assert st == binding.ERR_DEVICE_TIMEOUT
+        assert detail & 0x80000000
+    torch.cuda.synchronize()
+    # the context is still usable: a normal run afterwards is correct
+    check(run_gpu(A, B, M, N, K, **variant), A, B, M, N, K)
+
+
+def test_run_host_end_to_end():
+    M, N, K = 700, 600, 300
+    A, B = inputs.make_problem(M, N, K, "normal", seed=4)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hD = torch.zeros((M, N), dtype=torch.bfloat16).pin_memory()
+    dev = torch.device("cuda:0")
+    dA = torch.empty_like(A, device=dev)
+    dB = torch.empty_like(B, device=dev)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0) as g:
+        g.plan(M, N, K)
+        g.run_host(hA, hB, hD, dA, dB, dD)
+        torch.cuda.synchronize()
+        assert g.device_status()[0] == binding.OK
+    check(hD, A, B, M, N, K)
+
+
+def test_gemm_convenience_matches_oracle():
+    A, B = inputs.make_problem(384, 640, 320, "uniform", seed=8)
+    D = binding.gemm(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    check(D.cpu(), A, B, 384, 640, 320)

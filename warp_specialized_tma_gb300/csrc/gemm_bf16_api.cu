@@ -1,0 +1,552 @@
+// Host side of the C ABI declared in include/gemm_bf16.h: handle and options,
+// problem validation, plan (kernel variant, ring depth, grid), TMA tensor-map
+// encoding, launch, the host-operand end-to-end call and the watchdog status.
+#include "gemm_bf16.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "gemm_kernels.h"
+
+using namespace wstma;
+
+namespace {
+
+constexpr int kNumOptions = 12;
+constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
+
+struct Plan {
+    bool valid = false;
+    int64_t M = 0, N = 0, K = 0, lda = 0, ldb = 0, ldd = 0;
+    int pipeline = GEMM_BF16_PIPE_WS;
+    int cta_group = 1;
+    int persistent = 1;
+    int acc_buffers = 2;
+    int setmaxnreg = 1;
+    int stages = 0;
+    int raster_group = 8;
+    int epilogue_opt = 0;
+    int64_t tiles = 0;
+    int num_m_blocks = 0, num_n_blocks = 0, num_k_blocks = 0;
+    int grid_ctas = 0;
+    int threads = 0;
+    size_t smem = 0;
+    int regs = 0;
+    const void *fn = nullptr;
+    bool epi_tma_allowed = false;
+    int fault_skip = -1;
+    uint64_t watchdog_ns = 1000000000ull;
+};
+
+}  // namespace
+
+struct gemm_bf16 {
+    int device = 0;
+    int num_sms = 0;
+    size_t max_smem_optin = 0;
+    uint32_t *d_err = nullptr;
+    int64_t opt[kNumOptions];
+    Plan plan;
+    // tensor-map cache
+    bool maps_valid = false;
+    const void *mA = nullptr;
+    const void *mB = nullptr;
+    void *mD = nullptr;
+    CUtensorMap tmA, tmB, tmD;
+    cudaStream_t last_stream = nullptr;
+};
+
+namespace {
+
+int64_t default_option(int key)
+{
+    switch (key) {
+    case GEMM_BF16_OPT_PIPELINE: return GEMM_BF16_PIPE_WS;
+    case GEMM_BF16_OPT_CTA_GROUP: return 0;
+    case GEMM_BF16_OPT_PERSISTENT: return 1;
+    case GEMM_BF16_OPT_ACC_BUFFERS: return 2;
+    case GEMM_BF16_OPT_SETMAXNREG: return 1;
+    case GEMM_BF16_OPT_STAGES: return 0;
+    case GEMM_BF16_OPT_RASTER_GROUP: return 8;
+    case GEMM_BF16_OPT_EPILOGUE: return 0;
+    case GEMM_BF16_OPT_MAX_CTAS: return 0;
+    case GEMM_BF16_OPT_WATCHDOG_NS: return 1000000000LL;
+    case GEMM_BF16_OPT_FAULT_SKIP_LOAD: return -1;
+    default: return 0;
+    }
+}
+
+bool option_in_range(int key, int64_t v)
+{
+    switch (key) {
+    case GEMM_BF16_OPT_PIPELINE: return v >= 0 && v <= 2;
+    case GEMM_BF16_OPT_CTA_GROUP: return v >= 0 && v <= 2;
+    case GEMM_BF16_OPT_PERSISTENT: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_ACC_BUFFERS: return v == 1 || v == 2;
+    case GEMM_BF16_OPT_SETMAXNREG: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_STAGES: return v >= 0 && v <= kMaxStages;
+    case GEMM_BF16_OPT_RASTER_GROUP: return v >= 0 && v <= 4096;
+    case GEMM_BF16_OPT_EPILOGUE: return v >= 0 && v <= 2;
+    case GEMM_BF16_OPT_MAX_CTAS: return v >= 0 && v <= (1 << 20);
+    case GEMM_BF16_OPT_WATCHDOG_NS: return v >= 1000 && v <= 600LL * 1000000000LL;
+    case GEMM_BF16_OPT_FAULT_SKIP_LOAD: return v >= -1 && v <= kMaxDim;
+    default: return false;
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map: `cols` contiguous elements per row, `rows` rows,
+// `row_bytes` between rows; box = box_cols x box_rows with 128-byte swizzling;
+// out-of-bounds elements of a load read as zero.
+int encode_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
+              uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return GEMM_BF16_ERR_TENSORMAP;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_BF16_OK : GEMM_BF16_ERR_TENSORMAP;
+}
+
+int set_device(gemm_bf16_t h)
+{
+    return cudaSetDevice(h->device) == cudaSuccess ? GEMM_BF16_OK : GEMM_BF16_ERR_CUDA;
+}
+
+// Per-kernel attributes are set once per process and device.
+int prepare_kernel(const void *fn, size_t smem, int *regs)
+{
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, fn) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    *regs = a.numRegs;
+    return GEMM_BF16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+GEMM_BF16_API const char *gemm_bf16_strerror(int status)
+{
+    switch (status) {
+    case GEMM_BF16_OK: return "ok";
+    case GEMM_BF16_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_BF16_ERR_ALIGNMENT: return "alignment: TMA needs 16-byte aligned bases and row strides";
+    case GEMM_BF16_ERR_NOT_PLANNED: return "not planned: call gemm_bf16_plan first";
+    case GEMM_BF16_ERR_CUDA: return "a CUDA runtime call failed";
+    case GEMM_BF16_ERR_TENSORMAP: return "TMA tensor-map encoding failed";
+    case GEMM_BF16_ERR_DEVICE_TIMEOUT: return "device watchdog: a barrier wait ran out and the kernel returned early";
+    case GEMM_BF16_ERR_UNSUPPORTED: return "unsupported device or option combination";
+    default: return "unknown status";
+    }
+}
+
+GEMM_BF16_API const char *gemm_bf16_version(void) { return "gemm_bf16 1.0 sm_103a"; }
+
+GEMM_BF16_API int gemm_bf16_check_problem(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd)
+{
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (lda < K || ldb < K || ldd < N)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (lda > (int64_t(1) << 38) || ldb > (int64_t(1) << 38) || ldd > (int64_t(1) << 38))
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if ((lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0)
+        return GEMM_BF16_ERR_ALIGNMENT;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_create(int device, gemm_bf16_t *out)
+{
+    if (!out)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    *out = nullptr;
+    int dev = device;
+    if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || dev >= count) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    if (cudaSetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    int major = 0, minor = 0, sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3)
+        return GEMM_BF16_ERR_UNSUPPORTED;
+    gemm_bf16_t h = new (std::nothrow) gemm_bf16();
+    if (!h)
+        return GEMM_BF16_ERR_CUDA;
+    h->device = dev;
+    h->num_sms = sms;
+    h->max_smem_optin = (size_t)optin;
+    for (int k = 0; k < kNumOptions; ++k)
+        h->opt[k] = default_option(k);
+    if (cudaMalloc(&h->d_err, sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->d_err)
+            cudaFree(h->d_err);
+        delete h;
+        return GEMM_BF16_ERR_CUDA;
+    }
+    *out = h;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_destroy(gemm_bf16_t h)
+{
+    if (!h)
+        return GEMM_BF16_OK;
+    cudaSetDevice(h->device);
+    if (h->d_err)
+        cudaFree(h->d_err);
+    delete h;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_set_option(gemm_bf16_t h, int key, int64_t value)
+{
+    if (!h || key < 1 || key >= kNumOptions || !option_in_range(key, value))
+        return GEMM_BF16_ERR_INVALID_ARG;
+    h->opt[key] = value;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_get_option(gemm_bf16_t h, int key, int64_t *value)
+{
+    if (!h || !value || key < 1 || key >= kNumOptions)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    *value = h->opt[key];
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                 int64_t ldd)
+{
+    if (!h)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    h->plan.valid = false;
+    h->maps_valid = false;
+    int rc = gemm_bf16_check_problem(M, N, K, lda, ldb, ldd);
+    if (rc != GEMM_BF16_OK)
+        return rc;
+    if ((rc = set_device(h)) != GEMM_BF16_OK)
+        return rc;
+
+    Plan pl;
+    pl.M = M, pl.N = N, pl.K = K, pl.lda = lda, pl.ldb = ldb, pl.ldd = ldd;
+    pl.pipeline = (int)h->opt[GEMM_BF16_OPT_PIPELINE];
+    pl.persistent = (int)h->opt[GEMM_BF16_OPT_PERSISTENT];
+    pl.acc_buffers = (int)h->opt[GEMM_BF16_OPT_ACC_BUFFERS];
+    pl.setmaxnreg = (int)h->opt[GEMM_BF16_OPT_SETMAXNREG];
+    pl.raster_group = (int)h->opt[GEMM_BF16_OPT_RASTER_GROUP];
+    pl.epilogue_opt = (int)h->opt[GEMM_BF16_OPT_EPILOGUE];
+    pl.fault_skip = (int)h->opt[GEMM_BF16_OPT_FAULT_SKIP_LOAD];
+    pl.watchdog_ns = (uint64_t)h->opt[GEMM_BF16_OPT_WATCHDOG_NS];
+    pl.epi_tma_allowed = ((ldd * 2) % 16) == 0;
+
+    int cg = (int)h->opt[GEMM_BF16_OPT_CTA_GROUP];
+    const bool ws = pl.pipeline == GEMM_BF16_PIPE_WS;
+    if (!ws) {
+        if (cg == 2)
+            return GEMM_BF16_ERR_UNSUPPORTED;  // the ablation loops are single-CTA
+        cg = 1;
+        pl.persistent = 0;
+        pl.acc_buffers = 1;
+        pl.setmaxnreg = 0;
+    } else if (cg == 0) {
+        cg = 2;  // an SM pair per 256x256 tile halves each SM's operand traffic
+    }
+    pl.cta_group = cg;
+
+    pl.num_m_blocks = (int)((M + (int64_t)kBlockM * cg - 1) / ((int64_t)kBlockM * cg));
+    pl.num_n_blocks = (int)((N + kBlockN - 1) / kBlockN);
+    pl.num_k_blocks = (int)((K + kBlockK - 1) / kBlockK);
+    pl.tiles = (int64_t)pl.num_m_blocks * pl.num_n_blocks;
+    if (pl.tiles > kMaxDim / 2)
+        return GEMM_BF16_ERR_INVALID_ARG;
+
+    // ring depth: as deep as shared memory allows, or the requested depth
+    int max_stages = 0;
+    for (int s = kMaxStages; s >= 2; --s) {
+        const size_t need = ws ? ws_smem_bytes(cg, s) : nows_smem_bytes(s);
+        if (need <= h->max_smem_optin) {
+            max_stages = s;
+            break;
+        }
+    }
+    if (max_stages < 2)
+        return GEMM_BF16_ERR_UNSUPPORTED;
+    const int req = (int)h->opt[GEMM_BF16_OPT_STAGES];
+    if (req > max_stages || req == 1)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    pl.stages = req ? req : max_stages;
+    pl.smem = ws ? ws_smem_bytes(cg, pl.stages) : nows_smem_bytes(pl.stages);
+
+    if (ws) {
+        pl.fn = cg == 2 ? ws_kernel_c2(pl.setmaxnreg != 0) : ws_kernel_c1(pl.setmaxnreg != 0);
+        pl.threads = kWsThreads;
+    } else {
+        pl.fn = nows_kernel(pl.pipeline == GEMM_BF16_PIPE_MBAR_WAR);
+        pl.threads = kNowsThreads;
+    }
+    if ((rc = prepare_kernel(pl.fn, pl.smem, &pl.regs)) != GEMM_BF16_OK)
+        return rc;
+    // setmaxnreg.inc can only hand out registers the CTA was launched with.
+    if (ws && pl.setmaxnreg &&
+        pl.regs * kWsThreads < kProducerRegs * 128 + kConsumerRegs * (kWsThreads - 128))
+        return GEMM_BF16_ERR_UNSUPPORTED;
+
+    // grid
+    const int64_t max_ctas = h->opt[GEMM_BF16_OPT_MAX_CTAS];
+    if (!ws || !pl.persistent) {
+        pl.grid_ctas = (int)(pl.tiles * cg);
+    } else {
+        int64_t slots;
+        if (cg == 1) {
+            slots = h->num_sms;
+        } else {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((unsigned)(2 * std::max<int64_t>(1, h->num_sms / 2)), 1, 1);
+            cfg.blockDim = dim3(kWsThreads, 1, 1);
+            cfg.dynamicSmemBytes = pl.smem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, pl.fn, &cfg) != cudaSuccess || clusters < 1) {
+                cudaGetLastError();
+                clusters = h->num_sms / 2;
+            }
+            slots = (int64_t)clusters * 2;
+        }
+        int64_t ctas = std::min<int64_t>(pl.tiles * cg, slots);
+        if (max_ctas > 0)
+            ctas = std::min<int64_t>(ctas, std::max<int64_t>(cg, (max_ctas / cg) * cg));
+        pl.grid_ctas = (int)ctas;
+    }
+    if (!ws && max_ctas > 0)
+        return GEMM_BF16_ERR_UNSUPPORTED;  // one tile per CTA: the grid is fixed by the problem
+    pl.valid = true;
+    h->plan = pl;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info)
+{
+    if (!h || !info)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (!h->plan.valid)
+        return GEMM_BF16_ERR_NOT_PLANNED;
+    const Plan &p = h->plan;
+    std::memset(info, 0, sizeof(*info));
+    info->tiles = p.tiles;
+    info->k_blocks = p.num_k_blocks;
+    info->grid_ctas = p.grid_ctas;
+    info->threads_per_cta = p.threads;
+    info->cta_group = p.cta_group;
+    info->pipeline = p.pipeline;
+    info->persistent = p.persistent;
+    info->stages = p.stages;
+    info->acc_buffers = p.acc_buffers;
+    info->setmaxnreg = p.setmaxnreg;
+    info->tile_m = kBlockM * p.cta_group;
+    info->tile_n = kBlockN;
+    info->tile_k = kBlockK;
+    info->smem_bytes = (int32_t)p.smem;
+    info->num_sms = h->num_sms;
+    info->epilogue_tma_allowed = p.epi_tma_allowed ? 1 : 0;
+    info->raster_group = p.raster_group;
+    info->regs_per_thread = p.regs;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, void *D, void *stream)
+{
+    if (!h || !A || !B || !D)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (!h->plan.valid)
+        return GEMM_BF16_ERR_NOT_PLANNED;
+    const Plan &pl = h->plan;
+    if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
+        (reinterpret_cast<uintptr_t>(D) & 1u))
+        return GEMM_BF16_ERR_ALIGNMENT;
+    const bool d_aligned = (reinterpret_cast<uintptr_t>(D) & 15u) == 0;
+    bool epi_tma;
+    if (pl.epilogue_opt == 1) {
+        if (!pl.epi_tma_allowed || !d_aligned)
+            return GEMM_BF16_ERR_ALIGNMENT;
+        epi_tma = true;
+    } else if (pl.epilogue_opt == 2) {
+        epi_tma = false;
+    } else {
+        epi_tma = pl.epi_tma_allowed && d_aligned;
+    }
+    int rc = set_device(h);
+    if (rc != GEMM_BF16_OK)
+        return rc;
+
+    if (!h->maps_valid || h->mA != A || h->mB != B || h->mD != D) {
+        const uint32_t b_rows = (uint32_t)(kBlockN / pl.cta_group);
+        if ((rc = encode_2d(&h->tmA, A, (uint64_t)pl.K, (uint64_t)pl.M, (uint64_t)pl.lda * 2, kBlockK, kBlockM)) ||
+            (rc = encode_2d(&h->tmB, B, (uint64_t)pl.K, (uint64_t)pl.N, (uint64_t)pl.ldb * 2, kBlockK, b_rows))) {
+            h->maps_valid = false;
+            return rc;
+        }
+        if (pl.epi_tma_allowed && d_aligned) {
+            if ((rc = encode_2d(&h->tmD, D, (uint64_t)pl.N, (uint64_t)pl.M, (uint64_t)pl.ldd * 2, 64, 32))) {
+                h->maps_valid = false;
+                return rc;
+            }
+        } else {
+            std::memset(&h->tmD, 0, sizeof(h->tmD));  // never dereferenced on the masked path
+        }
+        h->mA = A, h->mB = B, h->mD = D;
+        h->maps_valid = true;
+    }
+
+    GemmParams prm;
+    prm.M = (int32_t)pl.M;
+    prm.N = (int32_t)pl.N;
+    prm.K = (int32_t)pl.K;
+    prm.num_m_blocks = pl.num_m_blocks;
+    prm.num_n_blocks = pl.num_n_blocks;
+    prm.num_k_blocks = pl.num_k_blocks;
+    prm.num_tiles = (int32_t)pl.tiles;
+    prm.raster_group = pl.raster_group;
+    prm.stages = pl.stages;
+    prm.acc_buffers = pl.acc_buffers;
+    prm.epi_tma = epi_tma ? 1 : 0;
+    prm.fault_skip_it = pl.fault_skip;
+    prm.ldd = pl.ldd;
+    prm.D = D;
+    prm.err = h->d_err;
+    prm.watchdog_ns = pl.watchdog_ns;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)pl.grid_ctas, 1, 1);
+    cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    if (pl.cta_group == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void *args[4] = {&h->tmA, &h->tmB, &h->tmD, &prm};
+    if (cudaLaunchKernelExC(&cfg, pl.fn, args) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    h->last_stream = static_cast<cudaStream_t>(stream);
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_run_host(gemm_bf16_t h, const void *hA, const void *hB, void *hD, void *dA, void *dB,
+                                     void *dD, void *stream)
+{
+    if (!h || !hA || !hB || !hD || !dA || !dB || !dD)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (!h->plan.valid)
+        return GEMM_BF16_ERR_NOT_PLANNED;
+    const Plan &pl = h->plan;
+    int rc = set_device(h);
+    if (rc != GEMM_BF16_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpy2DAsync(dA, pl.lda * 2, hA, pl.lda * 2, pl.K * 2, pl.M, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaMemcpy2DAsync(dB, pl.ldb * 2, hB, pl.ldb * 2, pl.K * 2, pl.N, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    if ((rc = gemm_bf16_run(h, dA, dB, dD, stream)) != GEMM_BF16_OK)
+        return rc;
+    if (cudaMemcpy2DAsync(hD, pl.ldd * 2, dD, pl.ldd * 2, pl.N * 2, pl.M, cudaMemcpyDeviceToHost, st) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail)
+{
+    if (!h)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    int rc = set_device(h);
+    if (rc != GEMM_BF16_OK)
+        return rc;
+    if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, h->d_err, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    if (detail)
+        *detail = w;
+    return w ? GEMM_BF16_ERR_DEVICE_TIMEOUT : GEMM_BF16_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+// Pieces shared by the warp-specialised kernel and the non-specialised
+// ablation kernels: the output-tile order and the epilogue store of one chunk.
+#pragma once
+
+#include "gemm_kernels.h"
+#include "ptx.cuh"
+
+namespace wstma {
+
+struct TileCoord {
+    int32_t mb;  // tile row
+    int32_t nb;  // tile column
+};
+
+// Linear output-tile index -> tile coordinates.  With raster_group G > 0 the
+// tiles are walked in bands of G tile rows, column by column inside a band, so
+// the tiles that run at the same time share A and B rows in L2; G = 0 is plain
+// row-major order.
+__device__ __forceinline__ TileCoord tile_coord(int32_t t, const GemmParams &p)
+{
+    if (p.raster_group <= 0)
+        return {t / p.num_n_blocks, t % p.num_n_blocks};
+    const int32_t span = p.raster_group * p.num_n_blocks;
+    const int32_t band = t / span;
+    const int32_t first = band * p.raster_group;
+    const int32_t rows = min(p.num_m_blocks - first, p.raster_group);
+    const int32_t r = t - band * span;
+    return {first + r % rows, r / rows};
+}
+
+// Epilogue of one chunk: the warp holds 32 rows x 64 fp32 columns of the
+// accumulator (thread = row; v0 = columns 0..31, v1 = columns 32..63).  They
+// are rounded to bf16 (nearest even), written to the warp's staging buffer in
+// the 128-byte-swizzled layout (16-byte unit u of row r at u ^ (r & 7)), and
+// stored to D[y .. y+31][x .. x+63] either by one TMA tensor store (which clips
+// rows >= M and columns >= N) or, when D's layout does not allow TMA, by
+// coalesced, masked st.global row by row.
+__device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v0)[32], const uint32_t (&v1)[32],
+                                                     uint32_t staging, int lane, bool tma_store,
+                                                     const CUtensorMap *tmD, int32_t x, int32_t y,
+                                                     const GemmParams &p)
+{
+    uint32_t pk[32];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        pk[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
+        pk[16 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
+    }
+
+    // The staging buffer is free once the previous TMA store finished reading it
+    // (or, on the masked path, once every lane finished its loads).
+    if (tma_store && lane == 0)
+        bulk_wait_read_all();
+    __syncwarp();
+
+    const uint32_t row = staging + (uint32_t)lane * 128u;
+    const uint32_t sw = (uint32_t)lane & 7u;
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u)
+        st_shared_v4(row + ((u ^ sw) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+
+    if (tma_store) {
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0 && x < p.N && y < p.M) {
+            tma_store_2d(tmD, staging, x, y);
+            bulk_commit_group();
+        }
+        return;
+    }
+
+    __syncwarp();
+    const int32_t col = x + 2 * lane;
+    const uint32_t unit = (uint32_t)lane >> 2;
+    const uint32_t word = ((uint32_t)lane & 3u) << 2;
+    uint16_t *const D = static_cast<uint16_t *>(p.D);
+    for (int r = 0; r < 32; ++r) {
+        const int32_t row_g = y + r;
+        if (row_g >= p.M)
+            break;
+        const uint32_t w = ld_shared_u32(staging + (uint32_t)r * 128u + ((unit ^ ((uint32_t)r & 7u)) << 4) + word);
+        if (col < p.N) {
+            uint16_t *dst = D + (int64_t)row_g * p.ldd + col;
+            if (col + 1 < p.N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                *reinterpret_cast<uint32_t *>(dst) = w;
+            } else {
+                dst[0] = (uint16_t)(w & 0xFFFFu);
+                if (col + 1 < p.N)
+                    dst[1] = (uint16_t)(w >> 16);
+            }
+        }
+    }
+}
+
+// Lane 0 waits on a barrier for the whole warp and broadcasts the outcome, so
+// that a watchdog give-up is warp-uniform before any .sync.aligned tcgen05 op.
+template <bool kClusterScope>
+__device__ __forceinline__ bool warp_wait(const WaitCtl &ctl, uint32_t bar, uint32_t parity, uint32_t role,
+                                          uint32_t where, int lane)
+{
+    uint32_t ok = 0;
+    if (lane == 0)
+        ok = ctl.wait<kClusterScope>(bar, parity, role, where) ? 1u : 0u;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    return ok != 0;
+}
+
+}  // namespace wstma

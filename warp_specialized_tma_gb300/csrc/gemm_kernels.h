@@ -1,0 +1,65 @@
+// Internal interface between the host library (gemm_bf16_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wstma {
+
+// Tile geometry shared by every kernel: a CTA owns a 128-row slab of the output
+// tile, a stage holds one 64-wide k-block (one 128-byte swizzle row per operand
+// row), and the accumulator is 256 fp32 columns of tensor memory.
+constexpr int kBlockM = 128;      // rows of D per CTA
+constexpr int kBlockN = 256;      // columns of D per tile (both modes)
+constexpr int kBlockK = 64;       // k per stage (64 bf16 = 128 bytes)
+constexpr int kEpiWarps = 8;      // two epilogue warpgroups in the WS kernel
+constexpr int kWsThreads = 384;   // WG0: producer / MMA / TMEM-alloc / spare warp; WG1-2: epilogue
+constexpr int kNowsThreads = 128; // the non-specialised ablation kernels
+constexpr int kStagingBytes = 32 * 64 * 2;  // per-warp epilogue staging: 32 rows x 64 bf16
+constexpr int kMaxStages = 8;
+
+// Producer / consumer register budgets for setmaxnreg (whole warpgroups).
+constexpr int kProducerRegs = 56;
+constexpr int kConsumerRegs = 224;
+
+struct GemmParams {
+    int32_t M, N, K;
+    int32_t num_m_blocks;   // tiles along M (tile height 128 * cta_group)
+    int32_t num_n_blocks;   // tiles along N (tile width 256)
+    int32_t num_k_blocks;   // ceil(K / 64)
+    int32_t num_tiles;
+    int32_t raster_group;   // 0 = row-major tile order
+    int32_t stages;
+    int32_t acc_buffers;    // 1 or 2 (WS only)
+    int32_t epi_tma;        // 1 = TMA-store epilogue, 0 = masked st.global
+    int32_t fault_skip_it;  // test hook, -1 = off
+    int64_t ldd;
+    void *D;
+    uint32_t *err;          // device status word (0 = fine)
+    uint64_t watchdog_ns;
+};
+
+// Dynamic shared memory a kernel needs for `stages` ring stages.
+inline size_t ws_smem_bytes(int cta_group, int stages)
+{
+    const size_t stage = (size_t)kBlockM * kBlockK * 2 + (size_t)(kBlockN / cta_group) * kBlockK * 2;
+    return 1024 /* alignment slack */ + (size_t)stages * stage + (size_t)kEpiWarps * kStagingBytes +
+           256 /* barriers, tmem slot, abort flag */;
+}
+
+inline size_t nows_smem_bytes(int stages)
+{
+    const size_t stage = (size_t)kBlockM * kBlockK * 2 + (size_t)kBlockN * kBlockK * 2;
+    return 1024 + (size_t)stages * stage + 4 * (size_t)kStagingBytes + 256;
+}
+
+// Kernel entry points, one per compiled variant.  All take
+// (CUtensorMap A, CUtensorMap B, CUtensorMap D, GemmParams).
+const void *ws_kernel_c1(bool setmaxnreg);
+const void *ws_kernel_c2(bool setmaxnreg);
+const void *nows_kernel(bool mbar_war);
+
+}  // namespace wstma

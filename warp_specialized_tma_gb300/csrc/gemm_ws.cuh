@@ -1,0 +1,294 @@
+// The persistent, warp-specialised GEMM kernel: D = A * B^T, bf16 in, fp32
+// accumulation in tensor memory, bf16 out.
+//
+// Roles (384 threads, one CTA per SM):
+//   warpgroup 0: warp 0 lane 0  = TMA producer
+//                warp 1 lane 0  = tcgen05 MMA issuer (leader CTA only in 2-CTA mode)
+//                warp 2         = tensor-memory allocator
+//                warp 3         = spare
+//   warpgroups 1, 2 (warps 4..11) = epilogue: TMEM -> registers -> bf16 -> smem -> TMA store
+//
+// Fuser issue #3941 ("Allow separate sub-DAG for load and compute warp groups
+// with warp-specialized circular buffering") gives the loop structure: the
+// producer runs ONE serial loop over the merged (output tile, cta-k) space and
+// the stage ring is indexed by that merged counter, while the compute side
+// keeps the tile loop and the k loop apart because the store has no k; the
+// load warps give registers back and the compute warps take them
+// (setmaxnreg).  Fuser PR #3446 ("Use mbarrier for WAR for circular
+// buffering") gives the ring: per stage a "full" mbarrier (TMA bytes landed)
+// and an "empty" mbarrier (the MMAs reading the stage completed).  On this
+// hardware the MMA is asynchronous and retires through tcgen05.commit, so the
+// "empty" arrive is the commit itself and the epilogue runs in its own warps
+// against two tensor-memory accumulators (accumulator-full / -empty barriers).
+// cutlass PR #3316 ("Fix race condition in 2SM TMEM alloc ...") gives the
+// 2-CTA rule: both CTAs pass a cluster barrier before the paired
+// tcgen05.alloc.
+#pragma once
+
+#include "gemm_common.cuh"
+
+namespace wstma {
+
+template <int CG, bool kSetMaxNReg>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const GemmParams p)
+{
+    static_assert(CG == 1 || CG == 2, "one CTA or an SM pair per tile");
+    constexpr bool kCluster = (CG == 2);
+    constexpr uint32_t kABytes = kBlockM * kBlockK * 2;          // 16 KiB: this CTA's 128 rows of A
+    constexpr uint32_t kBRows = kBlockN / CG;                    // rows of B this CTA loads
+    constexpr uint32_t kBBytes = kBRows * kBlockK * 2;
+    constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    constexpr uint32_t kTxBytes = kStageBytes * CG;              // bytes landing on the leader's full barrier
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kBlockM * CG, kBlockN);
+    constexpr int32_t kTileM = kBlockM * CG;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int S = p.stages;
+    const uint32_t stage0 = base;
+    const uint32_t staging0 = base + (uint32_t)S * kStageBytes;
+    const uint32_t full_bar = staging0 + kEpiWarps * kStagingBytes;
+    const uint32_t empty_bar = full_bar + 8u * S;
+    const uint32_t accf_bar = empty_bar + 8u * S;
+    const uint32_t acce_bar = accf_bar + 16u;
+    const uint32_t done_bar = acce_bar + 16u;
+    const uint32_t tmem_slot = done_bar + 8u;
+    const uint32_t abort_flag = tmem_slot + 4u;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = kCluster ? cluster_ctarank() : 0u;
+    const uint32_t acc_cols = (uint32_t)kBlockN * (uint32_t)p.acc_buffers;  // 256 or 512
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar + 8u * s, 1);
+            mbar_init(empty_bar + 8u * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar + 8u * a, 1);
+            mbar_init(acce_bar + 8u * a, kEpiWarps * CG);
+        }
+        mbar_init(done_bar, 1);
+        st_shared_u32(abort_flag, 0u);
+        fence_mbarrier_init();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmD);
+    }
+    // Both CTAs of a pair have initialised their barriers and are resident
+    // before any cross-CTA arrive, TMA completion or the paired allocation.
+    if constexpr (kCluster)
+        cluster_arrive_wait();
+    else
+        __syncthreads();
+
+    if (warp == 2) {
+        tmem_alloc<CG>(tmem_slot, acc_cols);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+
+    WaitCtl ctl;
+    ctl.abort_flag = abort_flag;
+    ctl.peer_abort_flag = kCluster ? mapa_shared(abort_flag, rank ^ 1u) : 0u;
+    ctl.err = p.err;
+    ctl.limit_ns = p.watchdog_ns;
+
+    const int32_t cluster_id = (int32_t)blockIdx.x / CG;
+    const int32_t num_clusters = (int32_t)gridDim.x / CG;
+
+    if (warp < 4) {
+        if constexpr (kSetMaxNReg)
+            setmaxnreg_dec<kProducerRegs>();
+
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer: one loop over (tile, k-block) ----------------
+            const uint32_t full_target = kCluster ? mapa_shared(full_bar, 0u) : full_bar;
+            int s = 0;
+            uint32_t ph = 0;
+            int32_t it = 0;
+            bool ok = true;
+            for (int32_t t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                const TileCoord tc = tile_coord(t, p);
+                const int32_t ya = tc.mb * kTileM + (int32_t)rank * kBlockM;
+                const int32_t yb = tc.nb * kBlockN + (int32_t)rank * (int32_t)kBRows;
+                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                    // wait until the MMAs that read this stage one lap ago have retired
+                    if (!ctl.wait<kCluster>(empty_bar + 8u * s, ph ^ 1u, kRoleProducer, (uint32_t)s)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it != p.fault_skip_it) {
+                        const uint32_t fb = full_target + 8u * s;
+                        if (!kCluster || rank == 0)
+                            mbar_arrive_expect_tx(full_bar + 8u * s, kTxBytes);
+                        const uint32_t sa = stage0 + (uint32_t)s * kStageBytes;
+                        const int32_t x = kb * kBlockK;
+                        if constexpr (kCluster) {
+                            tma_load_2d_pair(sa, &tmA, x, ya, fb);
+                            tma_load_2d_pair(sa + kABytes, &tmB, x, yb, fb);
+                        } else {
+                            tma_load_2d(sa, &tmA, x, ya, fb);
+                            tma_load_2d(sa + kABytes, &tmB, x, yb, fb);
+                        }
+                    }
+                    ++it;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // Teardown: the last S loads may still be in flight if a role gave up.
+            if (!kCluster || rank == 0) {
+                const int32_t n = it < S ? it : S;
+                for (int32_t d = 1; d <= n; ++d) {
+                    const int32_t j = it - d;
+                    if (j == p.fault_skip_it)
+                        continue;
+                    ctl.wait_drain<kCluster>(full_bar + 8u * (uint32_t)(j % S), (uint32_t)((j / S) & 1),
+                                             (uint32_t)(j % S));
+                }
+            } else if (ctl.aborted()) {
+                // The peer's loads complete on the leader's barriers, which this CTA
+                // cannot poll: give them a fixed grace period instead.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 50000ull) {
+                }
+            }
+        } else if (warp == 1 && lane == 0 && (!kCluster || rank == 0)) {
+            // ---------------- MMA issuer: tile { k-block { 4 x tcgen05.mma } } ----------------
+            const uint64_t adesc0 = smem_desc_sw128(stage0);
+            const uint64_t bdesc0 = smem_desc_sw128(stage0 + kABytes);
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t acc_ph = 0;
+            bool ok = true;
+            for (int32_t t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                // the epilogue has drained this accumulator (one lap ago)
+                if (!ctl.wait<kCluster>(acce_bar + 8u * acc, acc_ph ^ 1u, kRoleMmaAcc, (uint32_t)acc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBlockN);
+                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!ctl.wait<kCluster>(full_bar + 8u * s, ph, kRoleMmaFull, (uint32_t)s)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t step = (uint64_t)(((uint32_t)s * kStageBytes) >> 4);
+                    const uint64_t ad = adesc0 + step;
+                    const uint64_t bd = bdesc0 + step;
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk)
+                        mma_bf16<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    // the stage is free once these MMAs have read it
+                    if constexpr (kCluster)
+                        mma_commit_pair(empty_bar + 8u * s, (uint16_t)0x3);
+                    else
+                        mma_commit(empty_bar + 8u * s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                // the accumulator is complete once every MMA of the tile has retired
+                if constexpr (kCluster)
+                    mma_commit_pair(accf_bar + 8u * acc, (uint16_t)0x3);
+                else
+                    mma_commit(accf_bar + 8u * acc);
+                if (p.acc_buffers == 2) {
+                    acc ^= 1;
+                    if (acc == 0)
+                        acc_ph ^= 1u;
+                } else {
+                    acc_ph ^= 1u;
+                }
+            }
+            // no MMA may still be writing tensor memory when it is freed
+            if constexpr (kCluster)
+                mma_commit_pair(done_bar, (uint16_t)0x1);
+            else
+                mma_commit(done_bar);
+            ctl.wait_drain<kCluster>(done_bar, 0u, 0xFFFu);
+        }
+    } else {
+        if constexpr (kSetMaxNReg)
+            setmaxnreg_inc<kConsumerRegs>();
+
+        // ---------------- epilogue: tile { TMEM -> bf16 -> D } ----------------
+        const int ew = warp - 4;        // 0..7
+        const int q = warp & 3;         // tensor-memory lane quadrant this warp may read
+        const int half = ew >> 2;       // column half of the 256-wide accumulator
+        const uint32_t staging = staging0 + (uint32_t)ew * kStagingBytes;
+        const uint32_t acce_target = kCluster ? mapa_shared(acce_bar, 0u) : acce_bar;
+        const bool tma_store = p.epi_tma != 0;
+        int acc = 0;
+        uint32_t acc_ph = 0;
+        for (int32_t t = cluster_id; t < p.num_tiles; t += num_clusters) {
+            const TileCoord tc = tile_coord(t, p);
+            const int32_t y = tc.mb * kTileM + (int32_t)rank * kBlockM + q * 32;
+            const int32_t x0 = tc.nb * kBlockN + half * 128;
+            if (!warp_wait<kCluster>(ctl, accf_bar + 8u * acc, acc_ph, kRoleEpilogue, (uint32_t)acc, lane))
+                break;
+            tc_fence_after_sync();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBlockN + half * 128);
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v0[32], v1[32];
+                tmem_load_32x32(tbase + (uint32_t)(c * 64), v0);
+                tmem_load_32x32(tbase + (uint32_t)(c * 64 + 32), v1);
+                tmem_load_wait();
+                reg_fence(v0);
+                reg_fence(v1);
+                if (c == 1) {
+                    // every read of this accumulator is done: hand it back to the MMA warp
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (kCluster)
+                            mbar_arrive_cluster(acce_target + 8u * acc);
+                        else
+                            mbar_arrive(acce_bar + 8u * acc);
+                    }
+                }
+                epilogue_store_chunk(v0, v1, staging, lane, tma_store, &tmD, x0 + c * 64, y, p);
+            }
+            if (p.acc_buffers == 2) {
+                acc ^= 1;
+                if (acc == 0)
+                    acc_ph ^= 1u;
+            } else {
+                acc_ph ^= 1u;
+            }
+        }
+        if (lane == 0)
+            bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (kCluster)
+        cluster_arrive_wait();  // the peer is done with its reads and the leader's MMAs into it
+    if (warp == 2) {
+        tc_fence_after_sync();
+        tmem_dealloc<CG>(tmem_base, acc_cols);
+    }
+}
+
+}  // namespace wstma
