@@ -85,9 +85,11 @@ typedef enum gemm_bf16_option {
                                         0: one tile per CTA (grid = tiles) */
     GEMM_BF16_OPT_ACC_BUFFERS = 4,   /* tensor-memory accumulators per CTA: 2 (default) lets the
                                         epilogue of a tile overlap the next tile's main loop; 1 */
-    GEMM_BF16_OPT_SETMAXNREG = 5,    /* 1 (default): the producer/MMA warpgroup drops to 56
-                                        registers per thread and the epilogue warpgroups rise
-                                        to 224; 0: no rebalancing */
+    GEMM_BF16_OPT_SETMAXNREG = 5,    /* 1: the producer/MMA warpgroup drops to 56 registers per
+                                        thread and the epilogue warpgroups rise to 224;
+                                        0 (default): no rebalancing (the accumulator lives in
+                                        tensor memory, so no role needs more than the launch's
+                                        168 registers, and the 56-register limit spills) */
     GEMM_BF16_OPT_STAGES = 6,        /* stage-ring depth; 0 (default) = as deep as shared memory allows */
     GEMM_BF16_OPT_RASTER_GROUP = 7,  /* tile order: groups of this many tile rows walked column by
                                         column (default 8); 0 = plain row-major */

@@ -32,6 +32,11 @@ def _built():
     torch.cuda.synchronize()
 
 
+def pad8(K: int) -> int:
+    """Smallest leading dimension >= K whose rows start 16-byte aligned."""
+    return (K + 7) // 8 * 8
+
+
 def rms(t: torch.Tensor, K: int) -> float:
     v = t[:, :K].double()
     return float(v.pow(2).mean().sqrt())
@@ -42,9 +47,7 @@ def run_gpu(A, B, M, N, K, ldd=None, **opts):
     ldd = N if ldd is None else ldd
     dev = torch.device("cuda:0")
     dA, dB = A.to(dev), B.to(dev)
-    dD = torch.full((M, ldd), 0, dtype=torch.int16, device=dev)
-    dD.fill_(SENTINEL_BITS - 0x10000 if SENTINEL_BITS > 0x7FFF else SENTINEL_BITS)
-    dD = dD.view(torch.bfloat16)
+    dD = torch.full((M, ldd), SENTINEL_BITS, dtype=torch.int16, device=dev).view(torch.bfloat16)
     with binding.Gemm(0, **opts) as g:
         g.plan(M, N, K, A.shape[1], B.shape[1], ldd)
         g.run(dA, dB, dD)
@@ -108,8 +111,8 @@ MID = [(256, 256, 256), (300, 520, 200), (129, 257, 65), (640, 384, 1000), (1000
 @pytest.mark.parametrize("variant", [
     dict(cta_group=1),
     dict(cta_group=2),
-    dict(cta_group=1, setmaxnreg=0),
-    dict(cta_group=2, setmaxnreg=0),
+    dict(cta_group=1, setmaxnreg=1),
+    dict(cta_group=2, setmaxnreg=1),
     dict(cta_group=2, acc_buffers=1),
     dict(cta_group=1, persistent=0),
     dict(cta_group=2, persistent=0),
@@ -117,9 +120,9 @@ MID = [(256, 256, 256), (300, 520, 200), (129, 257, 65), (640, 384, 1000), (1000
     dict(pipeline=binding.PIPE_MBAR_WAR),
 ])
 def test_mid_shapes_all_variants(M, N, K, variant):
-    A, B = inputs.make_problem(M, N, K, "normal", seed=M + N + K)
+    A, B = inputs.make_problem(M, N, K, "normal", seed=M + N + K, lda=pad8(K), ldb=pad8(K))
     check(run_gpu(A, B, M, N, K, **variant), A, B, M, N, K)
-    Ai, Bi = inputs.make_problem(M, N, K, "int2", seed=M + N + K + 1)
+    Ai, Bi = inputs.make_problem(M, N, K, "int2", seed=M + N + K + 1, lda=pad8(K), ldb=pad8(K))
     check(run_gpu(Ai, Bi, M, N, K, **variant), Ai, Bi, M, N, K, exact=True)
 
 
@@ -134,9 +137,12 @@ def test_few_ctas_many_tiles_ring_wraps(cta_group, max_ctas, stages):
     check(D, A, B, M, N, K, exact=True)
 
 
-@pytest.mark.parametrize("epilogue,ldd", [(0, 520), (1, 520), (2, 520), (0, 523), (2, 528)])
-def test_epilogue_paths_and_padding(epilogue, ldd):
-    M, N, K = 333, 517, 96
+@pytest.mark.parametrize("N,epilogue,ldd", [
+    (517, 0, 520), (517, 1, 520), (517, 2, 520), (517, 0, 523), (517, 2, 528), (517, 1, 600),
+    (512, 1, 520), (520, 1, 600), (64, 1, 72), (1, 2, 1), (7, 0, 8)])
+def test_epilogue_paths_and_padding(N, epilogue, ldd):
+    # padding columns n >= N keep their sentinel on every path
+    M, K = 333, 96
     A, B = inputs.make_problem(M, N, K, "normal", seed=5)
     D = run_gpu(A, B, M, N, K, ldd=ldd, epilogue=epilogue)
     check(D, A, B, M, N, K)
@@ -231,6 +237,35 @@ def test_run_before_plan_and_bad_pointers():
         binding.gemm_bf16_destroy(h)
 
 
+def test_handles_with_different_ring_depths_interleave():
+    # the kernel's shared-memory limit is per function: plans of one handle must
+    # not stop another handle's deeper ring from launching
+    M, N, K = 512, 768, 256
+    A, B = inputs.make_problem(M, N, K, "int2", seed=31)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    deep = binding.Gemm(0)
+    deep.plan(M, N, K)
+    shallow = binding.Gemm(0, stages=3)
+    shallow.plan(M, N, K)
+    one = binding.Gemm(0, cta_group=1, stages=2)
+    one.plan(M, N, K)
+    try:
+        for _ in range(2):
+            deep.run(dA, dB, outs[0])
+            shallow.run(dA, dB, outs[1])
+            one.run(dA, dB, outs[2])
+        for g in (deep, shallow, one):
+            assert g.device_status()[0] == binding.OK
+        torch.cuda.synchronize()
+        for o in outs:
+            check(o.cpu(), A, B, M, N, K, exact=True)
+    finally:
+        for g in (deep, shallow, one):
+            g.close()
+
+
 def test_plan_info_reports_the_configuration():
     with binding.Gemm(0) as g:
         info = g.plan(8192, 8192, 8192)
@@ -264,7 +299,7 @@ def test_watchdog_reports_timeout_and_context_survives(variant):
 
 def test_run_host_end_to_end():
     M, N, K = 700, 600, 300
-    A, B = inputs.make_problem(M, N, K, "normal", seed=4)
+    A, B = inputs.make_problem(M, N, K, "normal", seed=4, lda=pad8(K), ldb=pad8(K))
     hA, hB = A.pin_memory(), B.pin_memory()
     hD = torch.zeros((M, N), dtype=torch.bfloat16).pin_memory()
     dev = torch.device("cuda:0")
@@ -272,7 +307,7 @@ def test_run_host_end_to_end():
     dB = torch.empty_like(B, device=dev)
     dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     with binding.Gemm(0) as g:
-        g.plan(M, N, K)
+        g.plan(M, N, K, pad8(K), pad8(K), N)
         g.run_host(hA, hB, hD, dA, dB, dD)
         torch.cuda.synchronize()
         assert g.device_status()[0] == binding.OK

@@ -30,7 +30,7 @@ struct Plan {
     int cta_group = 1;
     int persistent = 1;
     int acc_buffers = 2;
-    int setmaxnreg = 1;
+    int setmaxnreg = 0;
     int stages = 0;
     int raster_group = 8;
     int epilogue_opt = 0;
@@ -73,7 +73,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_CTA_GROUP: return 0;
     case GEMM_BF16_OPT_PERSISTENT: return 1;
     case GEMM_BF16_OPT_ACC_BUFFERS: return 2;
-    case GEMM_BF16_OPT_SETMAXNREG: return 1;
+    case GEMM_BF16_OPT_SETMAXNREG: return 0;
     case GEMM_BF16_OPT_STAGES: return 0;
     case GEMM_BF16_OPT_RASTER_GROUP: return 8;
     case GEMM_BF16_OPT_EPILOGUE: return 0;
@@ -141,10 +141,12 @@ int set_device(gemm_bf16_t h)
     return cudaSetDevice(h->device) == cudaSuccess ? GEMM_BF16_OK : GEMM_BF16_ERR_CUDA;
 }
 
-// Per-kernel attributes are set once per process and device.
-int prepare_kernel(const void *fn, size_t smem, int *regs)
+// The dynamic shared-memory limit is an attribute of the kernel function, shared
+// by every handle: it is raised to the device's opt-in maximum (not to this
+// plan's size), so plans of other handles with deeper rings still launch.
+int prepare_kernel(const void *fn, size_t max_smem, int *regs)
 {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;
     }
@@ -337,7 +339,7 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         pl.fn = nows_kernel(pl.pipeline == GEMM_BF16_PIPE_MBAR_WAR);
         pl.threads = kNowsThreads;
     }
-    if ((rc = prepare_kernel(pl.fn, pl.smem, &pl.regs)) != GEMM_BF16_OK)
+    if ((rc = prepare_kernel(pl.fn, h->max_smem_optin, &pl.regs)) != GEMM_BF16_OK)
         return rc;
     // setmaxnreg.inc can only hand out registers the CTA was launched with.
     if (ws && pl.setmaxnreg &&

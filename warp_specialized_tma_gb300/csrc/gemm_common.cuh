@@ -32,9 +32,12 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const GemmParams &p)
 // accumulator (thread = row; v0 = columns 0..31, v1 = columns 32..63).  They
 // are rounded to bf16 (nearest even), written to the warp's staging buffer in
 // the 128-byte-swizzled layout (16-byte unit u of row r at u ^ (r & 7)), and
-// stored to D[y .. y+31][x .. x+63] either by one TMA tensor store (which clips
-// rows >= M and columns >= N) or, when D's layout does not allow TMA, by
-// coalesced, masked st.global row by row.
+// stored to D[y .. y+31][x .. x+63] either by one TMA tensor store (which drops
+// rows >= M and whole 16-byte column groups beyond N) or by coalesced, masked
+// st.global row by row.  The masked path is taken when D's layout does not
+// allow TMA, and for the chunk holding a partial 16-byte group at column N
+// (N not a multiple of 8): a TMA store writes that group whole, which would
+// touch the padding columns n >= N.
 __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v0)[32], const uint32_t (&v1)[32],
                                                      uint32_t staging, int lane, bool tma_store,
                                                      const CUtensorMap *tmD, int32_t x, int32_t y,
@@ -59,7 +62,7 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v0)[32], c
     for (uint32_t u = 0; u < 8; ++u)
         st_shared_v4(row + ((u ^ sw) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
 
-    if (tma_store) {
+    if (tma_store && (x + 64 <= p.N || (p.N & 7) == 0)) {
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0 && x < p.N && y < p.M) {

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kNowsThreads, 1)
     ctl.abort_flag = abort_flag;
     ctl.peer_abort_flag = 0u;
     ctl.err = p.err;
-    ctl.limit_ns = p.watchdog_ns;
+    ctl.set_limit(p.watchdog_ns);
 
     const TileCoord tc = tile_coord((int32_t)blockIdx.x, p);
     const int32_t ya = tc.mb * kBlockM;
@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(kNowsThreads, 1)
     const int32_t KB = p.num_k_blocks;
 
     auto issue = [&](int32_t j) {
+        if (j == p.fault_skip_it)  // test hook: this stage never fills
+            return;
         const uint32_t s = (uint32_t)(j % S);
         const uint32_t sa = stage0 + s * kStageBytes;
         mbar_arrive_expect_tx(full_bar + 8u * s, kStageBytes);
@@ -114,11 +116,11 @@ __global__ void __launch_bounds__(kNowsThreads, 1)
         }
         // wait-load: every thread
         bool mine = ok && ctl.wait<false>(full_bar + 8u * s, ph, kRoleNoWs, s);
+        const uint64_t step = (uint64_t)((s * kStageBytes) >> 4);
+        const uint64_t ad = smem_desc_sw128(stage0) + step;
+        const uint64_t bd = smem_desc_sw128(stage0 + kABytes) + step;
         if (elected && mine) {
             tc_fence_after_sync();
-            const uint64_t step = (uint64_t)((s * kStageBytes) >> 4);
-            const uint64_t ad = smem_desc_sw128(stage0) + step;
-            const uint64_t bd = smem_desc_sw128(stage0 + kABytes) + step;
 #pragma unroll
             for (int kk = 0; kk < kBlockK / 16; ++kk)
                 mma_bf16<1>(tmem_base, ad + 2u * kk, bd + 2u * kk, kIdesc, (i | kk) != 0 ? 1u : 0u);
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(kNowsThreads, 1)
         const int32_t n = issued < S ? issued : S;
         for (int32_t d = 1; d <= n; ++d) {
             const int32_t j = issued - d;
+            if (j == p.fault_skip_it)
+                continue;
             ctl.wait_drain<false>(full_bar + 8u * (uint32_t)(j % S), (uint32_t)((j / S) & 1), (uint32_t)(j % S));
         }
         mma_commit(done_bar);

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t done_bar = acce_bar + 16u;
     const uint32_t tmem_slot = done_bar + 8u;
     const uint32_t abort_flag = tmem_slot + 4u;
+    const uint32_t go_flags = abort_flag + 4u;  // two words, see the epilogue
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     ctl.abort_flag = abort_flag;
     ctl.peer_abort_flag = kCluster ? mapa_shared(abort_flag, rank ^ 1u) : 0u;
     ctl.err = p.err;
-    ctl.limit_ns = p.watchdog_ns;
+    ctl.set_limit(p.watchdog_ns);
 
     const int32_t cluster_id = (int32_t)blockIdx.x / CG;
     const int32_t num_clusters = (int32_t)gridDim.x / CG;
@@ -109,6 +110,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if constexpr (kSetMaxNReg)
             setmaxnreg_dec<kProducerRegs>();
 
+        // The producer and MMA roles are single threads (lane 0 of their warp).
+        // Measured on GB300: a whole-warp loop with one issuing lane reacts to its
+        // barrier through a shuffle and starves the ring (producer) or adds
+        // per-k-block latency (MMA issuer).
         if (warp == 0 && lane == 0) {
             // ---------------- TMA producer: one loop over (tile, k-block) ----------------
             const uint32_t full_target = kCluster ? mapa_shared(full_bar, 0u) : full_bar;
@@ -126,12 +131,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         ok = false;
                         break;
                     }
+                    const uint32_t fb = full_target + 8u * s;
+                    const uint32_t sa = stage0 + (uint32_t)s * kStageBytes;
+                    const int32_t x = kb * kBlockK;
                     if (it != p.fault_skip_it) {
-                        const uint32_t fb = full_target + 8u * s;
                         if (!kCluster || rank == 0)
                             mbar_arrive_expect_tx(full_bar + 8u * s, kTxBytes);
-                        const uint32_t sa = stage0 + (uint32_t)s * kStageBytes;
-                        const int32_t x = kb * kBlockK;
                         if constexpr (kCluster) {
                             tma_load_2d_pair(sa, &tmA, x, ya, fb);
                             tma_load_2d_pair(sa + kABytes, &tmB, x, yb, fb);
@@ -173,6 +178,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             int acc = 0;
             uint32_t acc_ph = 0;
             bool ok = true;
+            bool ready = false;  // outcome of the look-ahead probe of ring slot (s, ph)
             for (int32_t t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
                 // the epilogue has drained this accumulator (one lap ago)
                 if (!ctl.wait<kCluster>(acce_bar + 8u * acc, acc_ph ^ 1u, kRoleMmaAcc, (uint32_t)acc)) {
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBlockN);
                 for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if (!ctl.wait<kCluster>(full_bar + 8u * s, ph, kRoleMmaFull, (uint32_t)s)) {
+                    if (!ready && !ctl.wait<kCluster>(full_bar + 8u * s, ph, kRoleMmaFull, (uint32_t)s)) {
                         ok = false;
                         break;
                     }
@@ -202,6 +208,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         s = 0;
                         ph ^= 1u;
                     }
+                    // non-blocking look at the next slot; its latency overlaps the
+                    // MMAs just issued
+                    ready = mbar_test_wait<kCluster>(full_bar + 8u * s, ph);
                 }
                 if (!ok)
                     break;
@@ -238,11 +247,24 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const bool tma_store = p.epi_tma != 0;
         int acc = 0;
         uint32_t acc_ph = 0;
+        uint32_t tile_parity = 0;
         for (int32_t t = cluster_id; t < p.num_tiles; t += num_clusters) {
             const TileCoord tc = tile_coord(t, p);
             const int32_t y = tc.mb * kTileM + (int32_t)rank * kBlockM + q * 32;
             const int32_t x0 = tc.nb * kBlockN + half * 128;
-            if (!warp_wait<kCluster>(ctl, accf_bar + 8u * acc, acc_ph, kRoleEpilogue, (uint32_t)acc, lane))
+            // One thread polls the accumulator barrier and posts the outcome; the
+            // other epilogue warps sleep on a named barrier instead of polling
+            // (every poll competes with the MMA issuer).  The outcome word
+            // alternates with the tile parity, so a warp that is one tile behind
+            // never reads the next tile's word.
+            const uint32_t go = go_flags + 4u * tile_parity;
+            if (ew == 0) {
+                const bool okw = warp_wait<kCluster>(ctl, accf_bar + 8u * acc, acc_ph, kRoleEpilogue, (uint32_t)acc, lane);
+                if (lane == 0)
+                    st_volatile_shared_u32(go, okw ? 1u : 0u);
+            }
+            named_barrier_sync(1, kEpiWarps * 32);
+            if (ld_volatile_shared_u32(go) == 0u)
                 break;
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBlockN + half * 128);
@@ -274,6 +296,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             } else {
                 acc_ph ^= 1u;
             }
+            tile_parity ^= 1u;
         }
         if (lane == 0)
             bulk_wait_all();

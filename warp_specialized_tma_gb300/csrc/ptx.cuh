@@ -105,15 +105,44 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-// One probe: true once the phase with parity `parity` has completed.
+// One potentially blocking probe: true once the phase with parity `parity`
+// has completed.  While the phase is open the thread is suspended in hardware
+// for up to `suspend_ns` (it resumes as soon as the phase completes), so a
+// waiting warp does not spin and take issue slots from the MMA issuer.
 template <bool kClusterScope>
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns)
 {
     uint32_t ok;
     if constexpr (kClusterScope) {
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(suspend_ns)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(suspend_ns)
+            : "memory");
+    }
+    return ok != 0;
+}
+
+// Non-blocking probe (never suspends the thread): used to look one ring slot
+// ahead so that the probe's latency overlaps the issue of the current MMAs.
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    if constexpr (kClusterScope) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(ok)
             : "r"(bar), "r"(parity)
@@ -121,7 +150,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     } else {
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(ok)
             : "r"(bar), "r"(parity)
@@ -142,6 +171,14 @@ struct WaitCtl {
     uint32_t peer_abort_flag;  // shared::cluster address of the peer's flag (0 = none)
     uint32_t *err;             // device status word
     uint64_t limit_ns;
+    uint32_t suspend_ns;       // per-probe hardware suspend bound (well below limit_ns)
+
+    __device__ __forceinline__ void set_limit(uint64_t ns)
+    {
+        limit_ns = ns;
+        const uint64_t s = ns / 8u;
+        suspend_ns = (uint32_t)(s < 10000000ull ? (s > 1000ull ? s : 1000ull) : 10000000ull);
+    }
 
     __device__ __forceinline__ bool aborted() const { return ld_volatile_shared_u32(abort_flag) != 0; }
 
@@ -157,7 +194,7 @@ struct WaitCtl {
     template <bool kClusterScope>
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, uint32_t role, uint32_t where) const
     {
-        if (mbar_try_wait<kClusterScope>(bar, parity))
+        if (mbar_try_wait<kClusterScope>(bar, parity, suspend_ns))
             return true;
         return wait_slow<kClusterScope>(bar, parity, role, where);
     }
@@ -167,15 +204,13 @@ struct WaitCtl {
     {
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t n = 1;; ++n) {
-            if (mbar_try_wait<kClusterScope>(bar, parity))
+            if (mbar_try_wait<kClusterScope>(bar, parity, suspend_ns))
                 return true;
-            if ((n & 15u) == 0u) {
-                if (aborted())
-                    return false;
-                if (globaltimer_ns() - t0 > limit_ns || n > (1u << 30)) {
-                    fail(role, where);
-                    return false;
-                }
+            if (aborted())
+                return false;
+            if (globaltimer_ns() - t0 > limit_ns || n > (1u << 30)) {
+                fail(role, where);
+                return false;
             }
         }
     }
@@ -187,9 +222,9 @@ struct WaitCtl {
     {
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t n = 0;; ++n) {
-            if (mbar_try_wait<kClusterScope>(bar, parity))
+            if (mbar_try_wait<kClusterScope>(bar, parity, suspend_ns))
                 return true;
-            if ((n & 15u) == 15u && (globaltimer_ns() - t0 > limit_ns || n > (1u << 30))) {
+            if (globaltimer_ns() - t0 > limit_ns || n > (1u << 30)) {
                 fail(kRoleDrainCode, where);
                 return false;
             }
@@ -208,6 +243,14 @@ enum : uint32_t {
     kRoleDrain = 5,      // teardown waiting for copies / MMAs in flight
     kRoleNoWs = 6        // non-specialised ablation kernels
 };
+
+// ---------------------------------------------------------------- named barriers
+// Hardware barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads
+// (a multiple of 32); waiting warps are descheduled, not polling.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ void cluster_arrive_wait()
