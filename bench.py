@@ -342,9 +342,11 @@ def run_ours(args):
     if st != binding.OK:
         raise RuntimeError(f"device watchdog tripped in the end-to-end loop: {detail:#x}")
 
+    # The GEMM kernel is timed alone (back-to-back launches of one kernel), so
+    # the roofline denominator is the measured burst bf16 figure.
     peaks, peak_src = load_peaks()
-    sustained = ms_total > 1000.0
-    peak = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops")
+    peak = peaks.get("bf16_tflops")
+    peak_sustained = peaks.get("bf16_tflops_sustained")
     kernel_tag = f"gemm_ws_c{info['cta_group']}"
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     traffic = profiled_traffic(kernel_tag, args.workload)
@@ -363,12 +365,13 @@ def run_ours(args):
             "config": workload_config(args.workload, info),
             "pct_of_dense_bf16_peak": {
                 "nominal_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
-                f"{peak_src}_{'sustained' if sustained else 'burst'}": 100.0 * value / world / peak,
+                f"{peak_src}_burst": 100.0 * value / world / peak,
+                f"{peak_src}_sustained": 100.0 * value / world / peak_sustained,
             },
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": kernel_tag, "kernel_ms": kernel_ms,
-                         "peak_source": f"{peak_src} {'bf16_tflops_sustained' if sustained else 'bf16_tflops'}"},
+                         "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * (M * K + N * K),
                     "d2h_bytes_per_step": 2 * M * N},
