@@ -185,6 +185,34 @@ GEMM_BF16_API int gemm_bf16_run_host(gemm_bf16_t h, const void *hA, const void *
  * stage or buffer). */
 GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail);
 
+/* GEMM for callers that cannot allocate device memory (no counterpart in the
+ * pages: this is a property of the library's interface, not of the method).
+ * Code being captured into a CUDA graph, runtimes whose pool owns all device
+ * memory, and loops that cannot afford an allocation's synchronisation cannot
+ * call gemm_bf16_create (it allocates); they call this instead.  It keeps no
+ * handle: it computes D = A * B^T exactly like gemm_bf16_run with the default
+ * options (same arguments and alignment rules, same kernel), with A, B, D and
+ * the stream supplied by the caller, and allocates nothing -- no cudaMalloc,
+ * cudaFree or allocating library call.
+ *
+ * Its scratch (the kernel watchdog's status word, 4 bytes) lives in a fixed
+ * 256-byte device array inside the library that every GPU loading the library
+ * holds until the process exits.  A call needing more scratch than that array
+ * is refused with INVALID_ARG before anything is enqueued.  Every call shares
+ * the array: each call clears the status word on `stream` before its launch,
+ * so calls that overlap on the GPU (different streams, or threads) race on it.
+ * If `status` is not NULL, the status word after the kernel is copied there on
+ * `stream` (0 = fine, else the watchdog word described at
+ * gemm_bf16_device_status); it is valid once the stream has synchronised.
+ *
+ * The first call on each device (with that device current) does a one-time
+ * set-up: it looks up the array's device address, sets the kernel's shared-
+ * memory limit and sizes the persistent grid.  Make that first call before any
+ * stream capture.  Uses the calling thread's current device. */
+GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                        int64_t ldd, const void *A, const void *B, void *D,
+                                        void *stream, uint32_t *status);
+
 /* Static, never-NULL description of a status code. */
 GEMM_BF16_API const char *gemm_bf16_strerror(int status);
 

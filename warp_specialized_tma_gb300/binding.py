@@ -58,6 +58,8 @@ _SIGNATURES = {
     "gemm_bf16_run": (ctypes.c_int, [_H, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "gemm_bf16_run_host": (ctypes.c_int, [_H] + [ctypes.c_void_p] * 7),
     "gemm_bf16_device_status": (ctypes.c_int, [_H, ctypes.POINTER(ctypes.c_uint32)]),
+    "gemm_bf16_run_noalloc": (ctypes.c_int, [ctypes.c_int64] * 6 + [ctypes.c_void_p] * 4
+                              + [ctypes.POINTER(ctypes.c_uint32)]),
     "gemm_bf16_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_bf16_version": (ctypes.c_char_p, []),
 }
@@ -165,6 +167,15 @@ def gemm_bf16_device_status(h):
     w = ctypes.c_uint32()
     st = load().gemm_bf16_device_status(h, ctypes.byref(w))
     return st, w.value
+
+
+def gemm_bf16_run_noalloc(M, N, K, lda, ldb, ldd, A: int, B: int, D: int, stream: int = 0, status=None) -> int:
+    """Allocation-free GEMM on the current device; `status` may be a ctypes.c_uint32
+    that receives the watchdog word once the stream has synchronised."""
+    return load().gemm_bf16_run_noalloc(int(M), int(N), int(K), int(lda), int(ldb), int(ldd),
+                                        ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(D),
+                                        ctypes.c_void_p(stream),
+                                        None if status is None else ctypes.byref(status))
 
 
 def gemm_bf16_strerror(status: int) -> str:
