@@ -99,10 +99,13 @@ typedef enum gemm_bf16_option {
                                         2 = masked coalesced st.global */
     GEMM_BF16_OPT_MAX_CTAS = 9,      /* upper bound on the persistent grid (0 = no bound) */
     GEMM_BF16_OPT_WATCHDOG_NS = 10,  /* limit of every in-kernel barrier wait, ns (default 1e9) */
-    GEMM_BF16_OPT_FAULT_SKIP_LOAD = 11 /* test hook: each CTA's producer skips its load at this
+    GEMM_BF16_OPT_FAULT_SKIP_LOAD = 11, /* test hook: each CTA's producer skips its load at this
                                           ring iteration, so the MMA warp's wait runs out and
                                           the kernel reports GEMM_BF16_ERR_DEVICE_TIMEOUT;
                                           -1 (default) = off */
+    GEMM_BF16_OPT_STAGE_GROUP = 12   /* ring stages released per MMA commit (WS only): 1 = every
+                                        k-block; 2 = stages pair up behind one "empty" barrier
+                                        (the ring depth must then be even); 0 (default) = 1 */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */
@@ -125,6 +128,7 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t epilogue_tma_allowed; /* 1 if ldd permits the TMA-store epilogue */
     int32_t raster_group;
     int32_t regs_per_thread;      /* registers per thread the kernel is launched with */
+    int32_t stage_group;          /* ring stages released per commit */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's

@@ -114,6 +114,8 @@ MID = [(256, 256, 256), (300, 520, 200), (129, 257, 65), (640, 384, 1000), (1000
     dict(cta_group=1, setmaxnreg=1),
     dict(cta_group=2, setmaxnreg=1),
     dict(cta_group=2, acc_buffers=1),
+    dict(cta_group=2, stage_group=1),
+    dict(cta_group=1, stage_group=1),
     dict(cta_group=1, persistent=0),
     dict(cta_group=2, persistent=0),
     dict(pipeline=binding.PIPE_SYNC_WAR),
@@ -127,13 +129,14 @@ def test_mid_shapes_all_variants(M, N, K, variant):
 
 
 @pytest.mark.parametrize("cta_group", [1, 2])
-@pytest.mark.parametrize("max_ctas,stages", [(2, 2), (4, 3), (6, 0)])
-def test_few_ctas_many_tiles_ring_wraps(cta_group, max_ctas, stages):
+@pytest.mark.parametrize("max_ctas,stages,group", [(2, 2, 2), (4, 3, 1), (6, 0, 0), (4, 4, 2), (2, 4, 1)])
+def test_few_ctas_many_tiles_ring_wraps(cta_group, max_ctas, stages, group):
     # few persistent CTAs walk many tiles: the ring and the accumulator
-    # barriers wrap across tile boundaries many times
+    # barriers wrap across tile boundaries many times; K = 520 gives 9 k-blocks
+    # per tile, so released stage pairs straddle tile boundaries
     M, N, K = 1100, 1300, 520
     A, B = inputs.make_problem(M, N, K, "int2", seed=21)
-    D = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stages=stages)
+    D = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stages=stages, stage_group=group)
     check(D, A, B, M, N, K, exact=True)
 
 

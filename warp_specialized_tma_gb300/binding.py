@@ -43,6 +43,7 @@ OPTIONS = {
     "max_ctas": 9,
     "watchdog_ns": 10,
     "fault_skip_load": 11,
+    "stage_group": 12,
 }
 
 # the C entry points and their signatures
@@ -85,6 +86,7 @@ class PlanInfo(ctypes.Structure):
         ("epilogue_tma_allowed", ctypes.c_int32),
         ("raster_group", ctypes.c_int32),
         ("regs_per_thread", ctypes.c_int32),
+        ("stage_group", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

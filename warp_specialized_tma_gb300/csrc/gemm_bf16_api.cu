@@ -20,7 +20,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 12;
+constexpr int kNumOptions = 13;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 
 struct Plan {
@@ -30,6 +30,7 @@ struct Plan {
     int cta_group = 1;
     int persistent = 1;
     int acc_buffers = 2;
+    int stage_group = 1;
     int setmaxnreg = 0;
     int stages = 0;
     int raster_group = 8;
@@ -80,6 +81,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_MAX_CTAS: return 0;
     case GEMM_BF16_OPT_WATCHDOG_NS: return 1000000000LL;
     case GEMM_BF16_OPT_FAULT_SKIP_LOAD: return -1;
+    case GEMM_BF16_OPT_STAGE_GROUP: return 0;
     default: return 0;
     }
 }
@@ -98,6 +100,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_MAX_CTAS: return v >= 0 && v <= (1 << 20);
     case GEMM_BF16_OPT_WATCHDOG_NS: return v >= 1000 && v <= 600LL * 1000000000LL;
     case GEMM_BF16_OPT_FAULT_SKIP_LOAD: return v >= -1 && v <= kMaxDim;
+    case GEMM_BF16_OPT_STAGE_GROUP: return v >= 0 && v <= 2;
     default: return false;
     }
 }
@@ -330,6 +333,17 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
     if (req > max_stages || req == 1)
         return GEMM_BF16_ERR_INVALID_ARG;
     pl.stages = req ? req : max_stages;
+    // k-blocks released per commit (WS only): 0 = automatic = 1 (measured
+    // fastest once the MMA issuer's probe is a try_wait; pairing stages costs
+    // ring slack)
+    const int g = (int)h->opt[GEMM_BF16_OPT_STAGE_GROUP];
+    if (!ws || g == 0) {
+        pl.stage_group = 1;
+    } else {
+        if (pl.stages % g != 0)
+            return GEMM_BF16_ERR_INVALID_ARG;
+        pl.stage_group = g;
+    }
     pl.smem = ws ? ws_smem_bytes(cg, pl.stages) : nows_smem_bytes(pl.stages);
 
     if (ws) {
@@ -403,6 +417,7 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->stages = p.stages;
     info->acc_buffers = p.acc_buffers;
     info->setmaxnreg = p.setmaxnreg;
+    info->stage_group = p.stage_group;
     info->tile_m = kBlockM * p.cta_group;
     info->tile_n = kBlockN;
     info->tile_k = kBlockK;
@@ -469,6 +484,7 @@ GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, voi
     prm.raster_group = pl.raster_group;
     prm.stages = pl.stages;
     prm.acc_buffers = pl.acc_buffers;
+    prm.stage_group = pl.stage_group;
     prm.epi_tma = epi_tma ? 1 : 0;
     prm.fault_skip_it = pl.fault_skip;
     prm.ldd = pl.ldd;

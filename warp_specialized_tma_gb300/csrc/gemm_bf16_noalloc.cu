@@ -196,6 +196,7 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     prm.raster_group = 8;
     prm.stages = ds->stages;
     prm.acc_buffers = 2;
+    prm.stage_group = 1;
     prm.epi_tma = epi_tma ? 1 : 0;
     prm.fault_skip_it = -1;
     prm.ldd = ldd;

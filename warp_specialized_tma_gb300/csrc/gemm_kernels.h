@@ -34,6 +34,7 @@ struct GemmParams {
     int32_t raster_group;   // 0 = row-major tile order
     int32_t stages;
     int32_t acc_buffers;    // 1 or 2 (WS only)
+    int32_t stage_group;    // k-blocks released per commit: 1, or 2 (stages pair up; S even) (WS only)
     int32_t epi_tma;        // 1 = TMA-store epilogue, 0 = masked st.global
     int32_t fault_skip_it;  // test hook, -1 = off
     int64_t ldd;

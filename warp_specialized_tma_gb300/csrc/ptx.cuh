@@ -133,32 +133,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
     return ok != 0;
 }
 
-// Non-blocking probe (never suspends the thread): used to look one ring slot
-// ahead so that the probe's latency overlaps the issue of the current MMAs.
-template <bool kClusterScope>
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    if constexpr (kClusterScope) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-    }
-    return ok != 0;
-}
-
 // ---------------------------------------------------------------- watchdog
 // Every spin-wait in the kernels goes through WaitCtl::wait: it gives up when
 // the CTA's abort flag is raised (another role already gave up) or when the
