@@ -103,9 +103,16 @@ typedef enum gemm_bf16_option {
                                           ring iteration, so the MMA warp's wait runs out and
                                           the kernel reports GEMM_BF16_ERR_DEVICE_TIMEOUT;
                                           -1 (default) = off */
-    GEMM_BF16_OPT_STAGE_GROUP = 12   /* ring stages released per MMA commit (WS only): 1 = every
+    GEMM_BF16_OPT_STAGE_GROUP = 12,  /* ring stages released per MMA commit (WS only): 1 = every
                                         k-block; 2 = stages pair up behind one "empty" barrier
                                         (the ring depth must then be even); 0 (default) = 1 */
+    GEMM_BF16_OPT_STREAM_K = 13      /* 1 (default): in the persistent WS kernel, when there is at
+                                        least one whole wave of tiles, the tiles that would form a
+                                        partial last wave are split along k over all resident SM
+                                        (pairs) -- each non-owner leaves an fp32
+                                        partial in a handle-owned workspace (128 KiB per CTA,
+                                        allocated by plan) that the owner of the tile's first
+                                        k-block adds before storing; 0: every tile runs whole */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */
@@ -129,6 +136,7 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t raster_group;
     int32_t regs_per_thread;      /* registers per thread the kernel is launched with */
     int32_t stage_group;          /* ring stages released per commit */
+    int32_t sk_tiles;             /* tiles split along k (stream-K); 0 = none */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's

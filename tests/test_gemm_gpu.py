@@ -140,6 +140,46 @@ def test_few_ctas_many_tiles_ring_wraps(cta_group, max_ctas, stages, group):
     check(D, A, B, M, N, K, exact=True)
 
 
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("M,N,K,max_ctas", [
+    (1024, 1024, 4096, 12),   # several split tiles, each over a few clusters
+    (1000, 900, 1000, 6),     # ragged edges and a k tail inside split tiles
+    (2048, 1536, 2560, 10),   # whole tiles plus split tiles
+    (512, 512, 8192, 6),      # long k, owners with several contributors
+])
+def test_stream_k_split_tiles_exact(cta_group, M, N, K, max_ctas):
+    A, B = inputs.make_problem(M, N, K, "int2", seed=M + K)
+    with binding.Gemm(0, cta_group=cta_group, max_ctas=max_ctas) as g:
+        info = g.plan(M, N, K)
+    assert info["sk_tiles"] > 0
+    D = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas)
+    check(D, A, B, M, N, K, exact=True)
+    # the split schedule and the whole-tile schedule agree bit for bit here
+    D0 = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stream_k=0)
+    assert torch.equal(D.view(torch.int16), D0.view(torch.int16))
+
+
+def test_stream_k_random_inputs_and_repeated_launches():
+    # flags carry a per-launch epoch: back-to-back launches on one handle must
+    # not read a previous launch's partials
+    M, N, K = 1536, 1280, 3072
+    A, B = inputs.make_problem(M, N, K, "normal", seed=77)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    outs = []
+    with binding.Gemm(0, max_ctas=8) as g:
+        assert g.plan(M, N, K)["sk_tiles"] > 0
+        for i in range(3):
+            D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            g.run(dA if i != 1 else dA * 2, dB, D)
+            outs.append(D)
+        assert g.device_status()[0] == binding.OK
+    torch.cuda.synchronize()
+    check(outs[0].cpu(), A, B, M, N, K)
+    check(outs[2].cpu(), A, B, M, N, K)
+    assert torch.equal(outs[1].cpu().float(), (outs[0].cpu().float() * 2))
+
+
 @pytest.mark.parametrize("N,epilogue,ldd", [
     (517, 0, 520), (517, 1, 520), (517, 2, 520), (517, 0, 523), (517, 2, 528), (517, 1, 600),
     (512, 1, 520), (520, 1, 600), (64, 1, 72), (1, 2, 1), (7, 0, 8)])

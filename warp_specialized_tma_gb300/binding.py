@@ -44,6 +44,7 @@ OPTIONS = {
     "watchdog_ns": 10,
     "fault_skip_load": 11,
     "stage_group": 12,
+    "stream_k": 13,
 }
 
 # the C entry points and their signatures
@@ -87,6 +88,7 @@ class PlanInfo(ctypes.Structure):
         ("raster_group", ctypes.c_int32),
         ("regs_per_thread", ctypes.c_int32),
         ("stage_group", ctypes.c_int32),
+        ("sk_tiles", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -12,7 +12,9 @@
 // process exits.
 //
 // It runs the same kernel as gemm_bf16_run with the default plan (SM-pair
-// 256x256 tiles, deepest ring, persistent grid, 1 s watchdog).  It calls no
+// 256x256 tiles, deepest ring, persistent grid, 1 s watchdog) except that every
+// tile runs whole: splitting tiles along k (stream-K) needs a partials
+// workspace of several MiB, which this entry point does not have.  It calls no
 // cudaMalloc, cudaFree or allocating library routine.
 #include "gemm_bf16.h"
 
@@ -203,6 +205,11 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     prm.D = D;
     prm.err = ds->scratch;  // word 0 of the shared scratch array
     prm.watchdog_ns = kWatchdogNs;
+    prm.sk_tiles = 0;  // stream-K needs a partials workspace, which this entry point does not have
+    prm.epoch = 1;
+    prm.sk_units = 0;
+    prm.workspace = nullptr;
+    prm.flags = nullptr;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the status word must start at zero for this call (the array keeps the

@@ -28,6 +28,61 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const GemmParams &p)
     return {first + r % rows, r / rows};
 }
 
+// ----------------------------------------------------------------- work items
+// One item of a cluster's work: k-blocks [kb0, kb1) of output tile `tile`.
+struct WorkItem {
+    int32_t tile;
+    int32_t kb0;
+    int32_t kb1;
+};
+
+// First stream-K unit of cluster c (unit u = k-block u % KB of tile u / KB):
+// the sk_units are split into C contiguous, near-equal ranges.
+__device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int32_t c, int32_t C)
+{
+    return (int64_t)c * p.sk_units / C;
+}
+
+// A cluster's work, in order: its contiguous share of the stream-K units
+// (tiles [0, sk_tiles), split along k), then the whole tiles sk_tiles + c,
+// sk_tiles + c + C, ...  Every role of the CTA walks the same sequence.
+struct WorkIter {
+    int64_t u, u_end, KB;
+    int32_t dp, C, T;
+
+    __device__ __forceinline__ void init(const GemmParams &p, int32_t cluster, int32_t nclusters)
+    {
+        KB = p.num_k_blocks;
+        C = nclusters;
+        T = p.num_tiles;
+        u = sk_begin(p, cluster, nclusters);
+        u_end = sk_begin(p, cluster + 1, nclusters);
+        dp = p.sk_tiles + cluster;
+    }
+
+    __device__ __forceinline__ bool next(WorkItem &w)
+    {
+        if (u < u_end) {
+            const int64_t t = u / KB;
+            const int64_t k0 = u - t * KB;
+            const int64_t k1 = (k0 + (u_end - u) < KB) ? k0 + (u_end - u) : KB;
+            w.tile = (int32_t)t;
+            w.kb0 = (int32_t)k0;
+            w.kb1 = (int32_t)k1;
+            u += k1 - k0;
+            return true;
+        }
+        if (dp < T) {
+            w.tile = dp;
+            w.kb0 = 0;
+            w.kb1 = (int32_t)KB;
+            dp += C;
+            return true;
+        }
+        return false;
+    }
+};
+
 // Epilogue of one chunk: the warp holds 32 rows x 64 fp32 columns of the
 // accumulator (thread = row; v0 = columns 0..31, v1 = columns 32..63).  They
 // are rounded to bf16 (nearest even), written to the warp's staging buffer in
@@ -93,6 +148,66 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v0)[32], c
             }
         }
     }
+}
+
+// ----------------------------------------------------------------- stream-K partials
+// A CTA's fp32 partial accumulator (128 rows x 256 columns) in its workspace
+// slot, laid out as the epilogue holds it: for warp ew, chunk c, the 64 values
+// of each lane's row go as 16 float4 groups j, and group j of all 32 lanes is
+// 512 contiguous bytes (coalesced stores and loads).
+__device__ __forceinline__ float4 *partial_addr(float *slot, int ew, int c, int j, int lane)
+{
+    return reinterpret_cast<float4 *>(slot) + (((ew * 2 + c) * 16 + j) * 32 + lane);
+}
+
+__device__ __forceinline__ void partial_store(float *slot, int ew, int c, int lane, const uint32_t (&v0)[32],
+                                              const uint32_t (&v1)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t *v = j < 8 ? &v0[4 * j] : &v1[4 * (j - 8)];
+        __stcg(partial_addr(slot, ew, c, j, lane),
+               make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                           __uint_as_float(v[3])));
+    }
+}
+
+__device__ __forceinline__ void partial_add(float *slot, int ew, int c, int lane, uint32_t (&v0)[32],
+                                            uint32_t (&v1)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float4 f = __ldcg(partial_addr(slot, ew, c, j, lane));
+        uint32_t *v = j < 8 ? &v0[4 * j] : &v1[4 * (j - 8)];
+        v[0] = __float_as_uint(__uint_as_float(v[0]) + f.x);
+        v[1] = __float_as_uint(__uint_as_float(v[1]) + f.y);
+        v[2] = __float_as_uint(__uint_as_float(v[2]) + f.z);
+        v[3] = __float_as_uint(__uint_as_float(v[3]) + f.w);
+    }
+}
+
+// Lane 0 waits (bounded) until a contributor's flag carries this launch's
+// epoch, then the whole warp proceeds; false if the wait gave up.
+__device__ __forceinline__ bool warp_wait_flag(const WaitCtl &ctl, const uint32_t *flag, uint32_t epoch, int lane)
+{
+    uint32_t ok = 1;
+    if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t n = 0; ld_acquire_gpu_u32(flag) != epoch; ++n) {
+            if (ctl.aborted()) {
+                ok = 0;
+                break;
+            }
+            if ((n & 63u) == 63u && (globaltimer_ns() - t0 > ctl.limit_ns || n > (1u << 30))) {
+                ctl.fail(kRoleFixup, 0);
+                ok = 0;
+                break;
+            }
+            __nanosleep(100);
+        }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    return ok != 0;
 }
 
 // Lane 0 waits on a barrier for the whole warp and broadcasts the outcome, so

@@ -41,7 +41,16 @@ struct GemmParams {
     void *D;
     uint32_t *err;          // device status word (0 = fine)
     uint64_t watchdog_ns;
+    // stream-K (WS only): tiles [0, sk_tiles) are split along k across all
+    // clusters, the other tiles are walked whole.  0 = off.
+    int32_t sk_tiles;
+    uint32_t epoch;         // this launch's flag value (never 0)
+    int64_t sk_units;       // sk_tiles * num_k_blocks
+    float *workspace;       // partials: per (cluster, rank) 128 x 256 fp32 = kPartialFloats
+    uint32_t *flags;        // per (cluster, rank): == epoch once that partial is complete
 };
+
+constexpr int kPartialFloats = kBlockM * kBlockN;  // one CTA's accumulator slice
 
 // Dynamic shared memory a kernel needs for `stages` ring stages.
 inline size_t ws_smem_bytes(int cta_group, int stages)

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kNowsThreads, 1)
     ctl.err = p.err;
     ctl.set_limit(p.watchdog_ns);
 
-    const TileCoord tc = tile_coord((int32_t)blockIdx.x, p);
+    const TileCoord tc = tile_coord((int32_t)blockIdx.x, p);  // one whole tile per CTA (no stream-K)
     const int32_t ya = tc.mb * kBlockM;
     const int32_t yb = tc.nb * kBlockN;
     const int32_t KB = p.num_k_blocks;

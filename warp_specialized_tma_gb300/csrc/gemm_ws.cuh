@@ -125,11 +125,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             uint32_t ph = 0;
             int32_t it = 0;
             bool ok = true;
-            for (int32_t t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-                const TileCoord tc = tile_coord(t, p);
+            WorkIter wi;
+            wi.init(p, cluster_id, num_clusters);
+            WorkItem w;
+            while (ok && wi.next(w)) {
+                const TileCoord tc = tile_coord(w.tile, p);
                 const int32_t ya = tc.mb * kTileM + (int32_t)rank * kBlockM;
                 const int32_t yb = tc.nb * kBlockN + (int32_t)rank * (int32_t)kBRows;
-                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     // wait until the MMAs that read this stage (group) one lap ago
                     // have retired; a group of G stages is released by one commit
                     if (((uint32_t)s & g_mask) == 0u &&
@@ -186,7 +189,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             uint32_t acc_ph = 0;
             bool ok = true;
             bool ready = false;  // outcome of the look-ahead probe of ring slot (s, ph)
-            for (int32_t t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+            WorkIter wi;
+            wi.init(p, cluster_id, num_clusters);
+            WorkItem w;
+            while (ok && wi.next(w)) {
                 // the epilogue has drained this accumulator (one lap ago)
                 if (!ctl.wait<kCluster>(acce_bar + 8u * acc, acc_ph ^ 1u, kRoleMmaAcc, (uint32_t)acc)) {
                     ok = false;
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBlockN);
-                for (int32_t kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!ready && !ctl.wait<kCluster>(full_bar + 8u * s, ph, kRoleMmaFull, (uint32_t)s)) {
                         ok = false;
                         break;
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const uint64_t bd = bdesc0 + step;
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk)
-                        mma_bf16<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        mma_bf16<CG>(d_tmem, ad + 2u * kk, bd + 2u * kk, kIdesc, (kb != w.kb0 || kk != 0) ? 1u : 0u);
                     // the stage group is free once its MMAs have read it.  One commit
                     // per G k-blocks: measured on GB300, a commit every 4 MMAs keeps the
                     // tensor pipe ~93% busy, one every 8 MMAs keeps it ~100% busy.
@@ -260,8 +266,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         int acc = 0;
         uint32_t acc_ph = 0;
         uint32_t tile_parity = 0;
-        for (int32_t t = cluster_id; t < p.num_tiles; t += num_clusters) {
-            const TileCoord tc = tile_coord(t, p);
+        WorkIter wi;
+        wi.init(p, cluster_id, num_clusters);
+        WorkItem w;
+        const int32_t KB = p.num_k_blocks;
+        while (wi.next(w)) {
+            const TileCoord tc = tile_coord(w.tile, p);
             const int32_t y = tc.mb * kTileM + (int32_t)rank * kBlockM + q * 32;
             const int32_t x0 = tc.nb * kBlockN + half * 128;
             // One thread polls the accumulator barrier and posts the outcome; the
@@ -279,6 +289,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (ld_volatile_shared_u32(go) == 0u)
                 break;
             tc_fence_after_sync();
+            // A stream-K item that does not start at k-block 0 is a contributor: it
+            // leaves its fp32 partial for the tile's owner.  The item holding
+            // k-block 0 of a split tile is the owner: it adds every contributor's
+            // partial before storing.  Each cluster contributes at most once (its
+            // first item), so its workspace slot is its own.
+            const bool contributor = w.kb0 > 0;
+            const bool owner = w.kb0 == 0 && w.kb1 < KB;
+            const int32_t slot_id = cluster_id * CG + (int32_t)rank;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBlockN + half * 128);
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
@@ -299,7 +317,34 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                             mbar_arrive(acce_bar + 8u * acc);
                     }
                 }
+                if (contributor) {
+                    partial_store(p.workspace + (size_t)slot_id * kPartialFloats, ew, c, lane, v0, v1);
+                    continue;
+                }
+                if (owner) {
+                    // contributors: the next clusters whose (non-empty) ranges start
+                    // inside this tile
+                    const int64_t tile_end = (int64_t)(w.tile + 1) * KB;
+                    for (int32_t c2 = cluster_id + 1; c2 < num_clusters; ++c2) {
+                        const int64_t b2 = sk_begin(p, c2, num_clusters);
+                        if (b2 >= tile_end)
+                            break;
+                        if (sk_begin(p, c2 + 1, num_clusters) == b2)
+                            continue;
+                        const int32_t slot2 = c2 * CG + (int32_t)rank;
+                        if (c == 0 && !warp_wait_flag(ctl, p.flags + slot2, p.epoch, lane))
+                            break;
+                        partial_add(p.workspace + (size_t)slot2 * kPartialFloats, ew, c, lane, v0, v1);
+                    }
+                }
                 epilogue_store_chunk(v0, v1, staging, lane, tma_store, &tmD, x0 + c * 64, y, p);
+            }
+            if (contributor) {
+                // publish the partial: every writer fences, then one thread raises the flag
+                __threadfence();
+                named_barrier_sync(2, kEpiWarps * 32);
+                if (ew == 0 && lane == 0)
+                    st_release_gpu_u32(p.flags + slot_id, p.epoch);
             }
             if (p.acc_buffers == 2) {
                 acc ^= 1;

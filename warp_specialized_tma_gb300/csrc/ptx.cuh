@@ -215,8 +215,22 @@ enum : uint32_t {
     kRoleMmaAcc = 3,     // MMA warp waiting for a drained accumulator
     kRoleEpilogue = 4,   // epilogue waiting for a finished accumulator
     kRoleDrain = 5,      // teardown waiting for copies / MMAs in flight
-    kRoleNoWs = 6        // non-specialised ablation kernels
+    kRoleNoWs = 6,       // non-specialised ablation kernels
+    kRoleFixup = 7       // stream-K owner waiting for a contributor's partial
 };
+
+// ---------------------------------------------------------------- global flags
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u32(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // ---------------------------------------------------------------- named barriers
 // Hardware barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads
