@@ -106,13 +106,18 @@ typedef enum gemm_bf16_option {
     GEMM_BF16_OPT_STAGE_GROUP = 12,  /* ring stages released per MMA commit (WS only): 1 = every
                                         k-block; 2 = stages pair up behind one "empty" barrier
                                         (the ring depth must then be even); 0 (default) = 1 */
-    GEMM_BF16_OPT_STREAM_K = 13      /* 1 (default): in the persistent WS kernel, when there is at
+    GEMM_BF16_OPT_STREAM_K = 13,     /* 1 (default): in the persistent WS kernel, when there is at
                                         least one whole wave of tiles, the tiles that would form a
                                         partial last wave are split along k over all resident SM
                                         (pairs) -- each non-owner leaves an fp32
                                         partial in a handle-owned workspace (128 KiB per CTA,
                                         allocated by plan) that the owner of the tile's first
                                         k-block adds before storing; 0: every tile runs whole */
+    GEMM_BF16_OPT_PDL = 14            /* 1 (default): launch with programmatic stream serialization,
+                                        so the kernel's prologue (barrier set-up, tensor-memory
+                                        allocation) overlaps the previous kernel on the stream; every
+                                        global access waits for that kernel (griddepcontrol.wait).
+                                        0: plain stream order */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */

@@ -309,6 +309,36 @@ def test_handles_with_different_ring_depths_interleave():
             g.close()
 
 
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_chained_gemms_on_one_stream_respect_order(pdl):
+    # D1 = A B^T, then D2 = D1 C^T and D3 = D2-free overwrite of D1, all
+    # enqueued back to back: with programmatic dependent launch each kernel's
+    # global accesses must still wait for the previous kernel.  Integer inputs
+    # keep both stages exact.
+    M, N, K, P = 768, 512, 64, 640
+    A, B = inputs.make_problem(M, N, K, "int2", seed=41)
+    g2 = torch.Generator().manual_seed(42)
+    C = inputs.make_operand(P, N, None, "int2", g2)
+    dev = torch.device("cuda:0")
+    dA, dB, dC = A.to(dev), B.to(dev), C.to(dev)
+    D1 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    D2 = torch.empty((M, P), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0, pdl=pdl) as g1, binding.Gemm(0, pdl=pdl) as g2h:
+        g1.plan(M, N, K)
+        g2h.plan(M, P, N)
+        for _ in range(5):
+            g1.run(dA, dB, D1)
+            g2h.run(D1, dC, D2)
+            D1.zero_()            # a plain kernel between our launches
+            g1.run(dA, dB, D1)
+        assert g1.device_status()[0] == binding.OK and g2h.device_status()[0] == binding.OK
+    torch.cuda.synchronize()
+    _, d1_ref = oracle.gemm_rows(inputs.bits(A), inputs.bits(B))
+    assert np.array_equal(inputs.bits(D1.cpu()), d1_ref)
+    _, d2_ref = oracle.gemm_rows(d1_ref, inputs.bits(C))
+    assert np.array_equal(inputs.bits(D2.cpu()), d2_ref)
+
+
 def test_plan_info_reports_the_configuration():
     with binding.Gemm(0) as g:
         info = g.plan(8192, 8192, 8192)

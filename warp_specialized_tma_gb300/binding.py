@@ -45,6 +45,7 @@ OPTIONS = {
     "fault_skip_load": 11,
     "stage_group": 12,
     "stream_k": 13,
+    "pdl": 14,
 }
 
 # the C entry points and their signatures

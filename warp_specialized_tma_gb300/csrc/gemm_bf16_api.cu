@@ -20,7 +20,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 14;
+constexpr int kNumOptions = 15;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 
 struct Plan {
@@ -89,6 +89,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_FAULT_SKIP_LOAD: return -1;
     case GEMM_BF16_OPT_STAGE_GROUP: return 0;
     case GEMM_BF16_OPT_STREAM_K: return 1;
+    case GEMM_BF16_OPT_PDL: return 1;
     default: return 0;
     }
 }
@@ -109,6 +110,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_FAULT_SKIP_LOAD: return v >= -1 && v <= kMaxDim;
     case GEMM_BF16_OPT_STAGE_GROUP: return v >= 0 && v <= 2;
     case GEMM_BF16_OPT_STREAM_K: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_PDL: return v == 0 || v == 1;
     default: return false;
     }
 }
@@ -550,19 +552,28 @@ GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, voi
     prm.epoch = h->epoch;
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned nattr = 0;
     cfg.gridDim = dim3((unsigned)pl.grid_ctas, 1, 1);
     cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     if (pl.cta_group == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = 2;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
     }
+    if (h->opt[GEMM_BF16_OPT_PDL]) {
+        // the kernel's prologue may overlap the previous kernel on the stream;
+        // griddepcontrol.wait orders every global access after it
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = nattr ? attr : nullptr;
+    cfg.numAttrs = nattr;
     void *args[4] = {&h->tmA, &h->tmB, &h->tmD, &prm};
     if (cudaLaunchKernelExC(&cfg, pl.fn, args) != cudaSuccess) {
         cudaGetLastError();

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kNowsThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+    grid_dependency_wait();  // A, B and D are touched only after this point
 
     WaitCtl ctl;
     ctl.abort_flag = abort_flag;

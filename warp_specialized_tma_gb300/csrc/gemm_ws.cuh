@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+    // Everything above touched only this CTA's shared and tensor memory, so it
+    // may overlap the previous kernel on the stream; from here on A, B, D and
+    // the workspace are read or written.
+    grid_dependency_wait();
 
     WaitCtl ctl;
     ctl.abort_flag = abort_flag;
@@ -162,6 +166,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     }
                 }
             }
+            // This CTA issues no more loads: the next kernel on the stream may begin
+            // launching (its CTAs start as this grid's CTAs exit).
+            grid_launch_dependents();
             // Teardown: the last S loads may still be in flight if a role gave up.
             if (!kCluster || rank == 0) {
                 const int32_t n = it < S ? it : S;

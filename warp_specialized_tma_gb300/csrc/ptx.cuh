@@ -232,6 +232,15 @@ __device__ __forceinline__ void st_release_gpu_u32(uint32_t *p, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream finishes.
+// griddepcontrol.wait blocks until that kernel has completed and its memory
+// is visible (a no-op when there is none); launch_dependents lets the next
+// kernel start its own prologue once every CTA of this grid has issued it.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- named barriers
 // Hardware barrier `id` (1..15; 0 is __syncthreads) over `nthreads` threads
 // (a multiple of 32); waiting warps are descheduled, not polling.
