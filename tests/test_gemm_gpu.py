@@ -339,6 +339,41 @@ def test_chained_gemms_on_one_stream_respect_order(pdl):
     assert np.array_equal(inputs.bits(D2.cpu()), d2_ref)
 
 
+def test_cuda_graph_capture_and_replay():
+    # plan outside the capture (it may allocate); run() only enqueues a launch
+    M, N, K = 2048, 1536, 1024
+    dev = torch.device("cuda:0")
+    A, B = inputs.make_problem(M, N, K, "int2", seed=51)
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.zeros((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0) as g:
+        g.plan(M, N, K)
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            g.run(dA, dB, dD)          # warm-up outside the capture
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            g.run(dA, dB, dD)
+        dD.zero_()
+        dA.copy_(A.to(dev) * -1)       # new inputs, same buffers
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        assert g.device_status()[0] == binding.OK
+    check(dD.cpu(), (A.float() * -1).to(torch.bfloat16), B, M, N, K, exact=True)
+
+
+@pytest.mark.parametrize("M,N,K", [(1 << 20, 384, 128), (256, 1 << 19, 64)])
+def test_very_large_m_or_n(M, N, K):
+    A, B = inputs.make_problem(M, N, K, "int2", seed=61)
+    D = run_gpu(A, B, M, N, K)
+    rows = np.array([0, 1, 255, 256, M // 2 + 7, M - 129, M - 1])
+    rows = rows[rows < M]
+    check(D, A, B, M, N, K, rows=rows, exact=True)
+
+
 def test_plan_info_reports_the_configuration():
     with binding.Gemm(0) as g:
         info = g.plan(8192, 8192, 8192)
