@@ -54,6 +54,11 @@ def _load():
         lib.oracle_gemm_rows.argtypes = [u16p, ctypes.c_int64, u16p, ctypes.c_int64,
                                          ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          i64p, ctypes.c_int64, f64p, u16p]
+        lib.oracle_gemm_fused_rows.restype = ctypes.c_int
+        lib.oracle_gemm_fused_rows.argtypes = [u16p, ctypes.c_int64, u16p, ctypes.c_int64,
+                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                               i64p, ctypes.c_int64, ctypes.c_double, ctypes.c_double,
+                                               u16p, ctypes.c_int64, u16p, f64p, u16p]
         lib.oracle_bf16_from_f64.restype = ctypes.c_uint16
         lib.oracle_bf16_from_f64.argtypes = [ctypes.c_double]
         lib.oracle_f64_from_bf16.restype = ctypes.c_double
@@ -113,6 +118,52 @@ def gemm_rows(A: np.ndarray, B: np.ndarray, K: int | None = None, rows=None):
                               _ptr(refbf16, ctypes.c_uint16))
     if rc != 0:
         raise ValueError("oracle_gemm_rows rejected its arguments")
+    return ref64, refbf16
+
+
+def gemm_fused_rows(A: np.ndarray, B: np.ndarray, alpha: float, beta: float, C=None, bias=None,
+                    K: int | None = None, rows=None):
+    """Rows of D = alpha * (A * B^T) + beta * C + bias (bias broadcast over rows).
+
+    ``C`` is an (M, ldc) uint16 array of bf16 patterns or None; ``bias`` an (N,)
+    uint16 array or None; alpha and beta are the fp32 values the GPU receives
+    (pass Python floats that are exactly fp32, e.g. via numpy.float32).
+    Returns ``(ref64, refbf16)`` like :func:`gemm_rows`.
+    """
+    lib = _load()
+    A = np.ascontiguousarray(_u16(A))
+    B = np.ascontiguousarray(_u16(B))
+    M, lda = A.shape
+    N, ldb = B.shape
+    K = min(lda, ldb) if K is None else int(K)
+    if C is not None:
+        C = np.ascontiguousarray(_u16(C))
+        if C.shape[0] != M or C.shape[1] < N:
+            raise ValueError("C must be M x ldc with ldc >= N")
+        ldc = C.shape[1]
+    else:
+        ldc = 0
+    if bias is not None:
+        bias = np.ascontiguousarray(_u16(bias)).reshape(-1)
+        if bias.size < N:
+            raise ValueError("bias must have N entries")
+    if rows is None:
+        rows_arr = None
+        nrows = M
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.size
+    ref64 = np.empty((nrows, N), dtype=np.float64)
+    refbf16 = np.empty((nrows, N), dtype=np.uint16)
+    rc = lib.oracle_gemm_fused_rows(
+        _ptr(A, ctypes.c_uint16), lda, _ptr(B, ctypes.c_uint16), ldb, M, N, K,
+        None if rows_arr is None else _ptr(rows_arr, ctypes.c_int64), nrows,
+        float(alpha), float(beta),
+        None if C is None else _ptr(C, ctypes.c_uint16), ldc,
+        None if bias is None else _ptr(bias, ctypes.c_uint16),
+        _ptr(ref64, ctypes.c_double), _ptr(refbf16, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError("oracle_gemm_fused_rows rejected its arguments")
     return ref64, refbf16
 
 

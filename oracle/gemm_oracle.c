@@ -149,6 +149,55 @@ int oracle_gemm_rows(const uint16_t *A, int64_t lda,
     return 0;
 }
 
+/* Rows of the fused form  D = alpha * (A * B^T) + beta * C + bias.
+ *
+ * The pages' epilogue (Fuser issue #3941, Pseudo-code: convert the fp32 sums
+ * and store) is the place a GEMM fuses its element-wise tail; this is the
+ * plain definition of that tail.  Every term is formed in fp64 from the same
+ * inputs the GPU gets -- alpha and beta as given (fp32 values, exact in fp64),
+ * C[m][n] and bias[n] widened from bf16 -- and the total is rounded ONCE to
+ * bf16.  C (row pitch ldc) and bias may be NULL, meaning 0.  Outputs as in
+ * oracle_gemm_rows (ref64 is the unrounded fp64 value).  Returns 0 or -1. */
+int oracle_gemm_fused_rows(const uint16_t *A, int64_t lda,
+                           const uint16_t *B, int64_t ldb,
+                           int64_t M, int64_t N, int64_t K,
+                           const int64_t *rows, int64_t nrows,
+                           double alpha, double beta,
+                           const uint16_t *C, int64_t ldc, const uint16_t *bias,
+                           double *ref64, uint16_t *refbf16)
+{
+    if (M < 0 || N < 0 || K < 0 || nrows < 0 || lda < K || ldb < K || (C && ldc < N))
+        return -1;
+    if (rows == NULL && nrows != M)
+        return -1;
+    if (rows != NULL)
+        for (int64_t i = 0; i < nrows; ++i)
+            if (rows[i] < 0 || rows[i] >= M)
+                return -1;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        const uint16_t *a = A + m * lda;
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t *b = B + n * ldb;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += oracle_f64_from_bf16(a[k]) * oracle_f64_from_bf16(b[k]);
+            double v = alpha * acc;
+            if (C)
+                v += beta * oracle_f64_from_bf16(C[m * ldc + n]);
+            if (bias)
+                v += oracle_f64_from_bf16(bias[n]);
+            if (ref64)
+                ref64[i * N + n] = v;
+            if (refbf16)
+                refbf16[i * N + n] = oracle_bf16_from_f64(v);
+        }
+    }
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -252,3 +252,61 @@ def test_bad_row_rejected():
     A, B = inputs.make_problem(4, 4, 8, "normal", seed=1)
     with pytest.raises(ValueError):
         oracle.gemm_rows(inputs.bits(A), inputs.bits(B), rows=[4])
+
+
+# ---------------------------------------------------------------------------
+# Fused epilogue D = alpha * (A B^T) + beta * C + bias
+# ---------------------------------------------------------------------------
+def test_fused_reduces_to_plain_gemm():
+    A, B = inputs.make_problem(23, 41, 57, "normal", seed=13)
+    C = inputs.make_operand(23, 41, None, "normal", torch.Generator().manual_seed(14))
+    plain64, plainbf = oracle.gemm_rows(inputs.bits(A), inputs.bits(B))
+    f64, fbf = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 1.0, 0.0, C=inputs.bits(C))
+    assert np.array_equal(f64, plain64) and np.array_equal(fbf, plainbf)
+    f64, fbf = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 1.0, 0.0)
+    assert np.array_equal(fbf, plainbf)
+
+
+def test_fused_alpha_zero_gives_c_and_bias_exactly():
+    g = torch.Generator().manual_seed(15)
+    A, B = inputs.make_problem(17, 30, 40, "normal", seed=16)
+    C = inputs.make_operand(17, 32, None, "normal", g)          # ldc = 32 > N = 30
+    bias = inputs.make_operand(1, 30, None, "uniform", g).reshape(-1)
+    _, d = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 0.0, 1.0, C=inputs.bits(C))
+    assert np.array_equal(d, inputs.bits(C)[:, :30])
+    _, d = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 0.0, 0.0, bias=inputs.bits(bias))
+    assert np.array_equal(d, np.broadcast_to(inputs.bits(bias), (17, 30)))
+
+
+def test_fused_bruteforce_tiny_exact():
+    rng = np.random.default_rng(200)
+    alpha, beta = 0.75, -1.5                                     # exact binary fractions
+    for M in (1, 3, 5):
+        for N in (1, 2, 6):
+            for K in (1, 4, 7):
+                A = random_bf16_bits(rng, (M, K))
+                B = random_bf16_bits(rng, (N, K))
+                C = random_bf16_bits(rng, (M, N + 2))
+                bias = random_bf16_bits(rng, (N,))
+                ref64, refbf = oracle.gemm_fused_rows(A, B, alpha, beta, C=C, bias=bias, K=K)
+                dot = _exact_gemm(A, B, K)
+                for m in range(M):
+                    for n in range(N):
+                        want = (Fraction(alpha) * dot[m][n] + Fraction(beta) * bf16_value(int(C[m, n]))
+                                + bf16_value(int(bias[n])))
+                        assert Fraction(float(ref64[m, n])) == want, (M, N, K, m, n)
+                        assert int(refbf[m, n]) == exact_rne_bf16(want), (M, N, K, m, n)
+
+
+def test_fused_integer_closed_form():
+    A, B = inputs.make_problem(19, 27, 90, "int2", seed=17)
+    g = torch.Generator().manual_seed(18)
+    C = inputs.make_operand(19, 27, None, "int2", g)
+    bias = inputs.make_operand(1, 27, None, "int2", g).reshape(-1)
+    ref64, refbf = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 2.0, -3.0,
+                                          C=inputs.bits(C), bias=inputs.bits(bias))
+    exact = (2 * (A.to(torch.int64).numpy() @ B.to(torch.int64).numpy().T)
+             - 3 * C.to(torch.int64).numpy() + bias.to(torch.int64).numpy()[None, :])
+    assert np.array_equal(ref64, exact.astype(np.float64))
+    want = np.array([[exact_rne_bf16(Fraction(int(v))) for v in row] for row in exact], dtype=np.uint16)
+    assert np.array_equal(refbf, want)
