@@ -190,6 +190,22 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
 GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, void *D,
                                 void *stream);
 
+/* Fused-epilogue variant:
+ *     D[m][n] = bf16( alpha * sum_k A[m][k] * B[n][k] + beta * C[m][n] + bias[n] )
+ * computed in fp32 in the epilogue and rounded once to bf16 (Fuser issue #3941,
+ * Pseudo-code: the epilogue is where the fp32 sums are converted and stored, the
+ * one place a GEMM fuses element-wise work).
+ *   C    : device, M rows of ldc bf16 (ldc >= N), or NULL (then beta is ignored);
+ *          C may be D itself (ldc == ldd) for an in-place D = alpha*AB^T + beta*D;
+ *          16-byte-aligned rows (C base and ldc*2) load as vectors, other layouts
+ *          element by element.
+ *   bias : device, N bf16 values broadcast over rows, or NULL.
+ * Same planning, layouts and error rules as gemm_bf16_run; additionally
+ * INVALID_ARG if ldc < N, ALIGNMENT if C or bias is not 2-byte aligned. */
+GEMM_BF16_API int gemm_bf16_run_fused(gemm_bf16_t h, const void *A, const void *B, void *D,
+                                      const void *C, int64_t ldc, const void *bias,
+                                      float alpha, float beta, void *stream);
+
 /* End-to-end variant with HOST operands: enqueues on `stream` the copies
  * hA -> dA and hB -> dB (the M x K and N x K sub-matrices, row pitches lda and
  * ldb), the GEMM on dA, dB, dD, and the copy of the M x N result dD -> hD (row

@@ -374,6 +374,78 @@ def test_very_large_m_or_n(M, N, K):
     check(D, A, B, M, N, K, rows=rows, exact=True)
 
 
+def run_fused_gpu(A, B, M, N, K, C=None, bias=None, alpha=1.0, beta=0.0, ldd=None, inplace=False, **opts):
+    ldd = N if ldd is None else ldd
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    if inplace:
+        dD = C.to(dev).clone()
+        dC = dD
+    else:
+        dD = torch.full((M, ldd), SENTINEL_BITS, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        dC = None if C is None else C.to(dev)
+    dbias = None if bias is None else bias.to(dev)
+    with binding.Gemm(0, **opts) as g:
+        g.plan(M, N, K, A.shape[1], B.shape[1], ldd)
+        g.run_fused(dA, dB, dD, dC, dbias, alpha, beta)
+        assert g.device_status()[0] == binding.OK
+    torch.cuda.synchronize()
+    return dD.cpu()
+
+
+@pytest.mark.parametrize("variant", [dict(), dict(cta_group=1), dict(max_ctas=14),
+                                     dict(pipeline=binding.PIPE_MBAR_WAR), dict(epilogue=2)])
+def test_fused_epilogue_exact_integers(variant):
+    M, N, K = 1100, 900, 2560
+    A, B = inputs.make_problem(M, N, K, "int2", seed=71)
+    g = torch.Generator().manual_seed(72)
+    C = inputs.make_operand(M, N, None, "int2", g)
+    bias = inputs.make_operand(1, N, None, "int2", g).reshape(-1)
+    D = run_fused_gpu(A, B, M, N, K, C=C, bias=bias, alpha=2.0, beta=-3.0, **variant)
+    _, refbf = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 2.0, -3.0, C=inputs.bits(C),
+                                      bias=inputs.bits(bias))
+    assert np.array_equal(inputs.bits(D), refbf)
+
+
+@pytest.mark.parametrize("case", ["all", "c_only", "bias_only", "alpha_only", "odd_ldc", "inplace"])
+def test_fused_epilogue_random_values(case):
+    M, N, K = 777, 520, 1000
+    A, B = inputs.make_problem(M, N, K, "normal", seed=73)
+    g = torch.Generator().manual_seed(74)
+    ldc = 523 if case == "odd_ldc" else N
+    C = inputs.make_operand(M, N, ldc, "normal", g) if case in ("all", "c_only", "odd_ldc", "inplace") else None
+    bias = inputs.make_operand(1, N, None, "uniform", g).reshape(-1) if case in ("all", "bias_only") else None
+    alpha = float(np.float32(0.625 if case != "alpha_only" else -1.375))
+    beta = float(np.float32(1.25))
+    D = run_fused_gpu(A, B, M, N, K, C=C, bias=bias, alpha=alpha, beta=beta,
+                      ldd=ldc if case == "inplace" else None, inplace=(case == "inplace"))
+    ref64, _ = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), alpha, beta,
+                                      C=None if C is None else inputs.bits(C),
+                                      bias=None if bias is None else inputs.bits(bias))
+    got = D[:, :N].double().numpy()
+    tol = (4e-3 * np.abs(ref64) + 2e-3 * math.sqrt(K) * rms(A, K) * rms(B, K) * abs(alpha) + 1e-6)
+    assert np.all(np.abs(got - ref64) <= tol)
+    if case == "inplace":
+        # columns beyond N keep C's own values
+        assert torch.equal(D[:, N:].view(torch.int16), C[:, N:].view(torch.int16))
+
+
+def test_fused_rejects_bad_arguments():
+    dev = torch.device("cuda:0")
+    buf = torch.zeros(1 << 16, dtype=torch.bfloat16, device=dev)
+    p = buf.data_ptr()
+    st, h = binding.gemm_bf16_create(0)
+    try:
+        assert binding.gemm_bf16_run_fused(h, p, p, p, p, 16, 0, 1.0, 1.0) == binding.ERR_NOT_PLANNED
+        assert binding.gemm_bf16_plan(h, 16, 16, 16, 16, 16, 16) == binding.OK
+        assert binding.gemm_bf16_run_fused(h, p, p, p, p, 8, 0, 1.0, 1.0) == binding.ERR_INVALID_ARG
+        assert binding.gemm_bf16_run_fused(h, p, p, p, p + 1, 16, 0, 1.0, 1.0) == binding.ERR_ALIGNMENT
+        assert binding.gemm_bf16_run_fused(h, p, p, p, 0, 0, p + 1, 1.0, 1.0) == binding.ERR_ALIGNMENT
+    finally:
+        torch.cuda.synchronize()
+        binding.gemm_bf16_destroy(h)
+
+
 def test_plan_info_reports_the_configuration():
     with binding.Gemm(0) as g:
         info = g.plan(8192, 8192, 8192)

@@ -60,6 +60,9 @@ _SIGNATURES = {
     "gemm_bf16_plan_info": (ctypes.c_int, [_H, ctypes.c_void_p]),
     "gemm_bf16_run": (ctypes.c_int, [_H, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "gemm_bf16_run_host": (ctypes.c_int, [_H] + [ctypes.c_void_p] * 7),
+    "gemm_bf16_run_fused": (ctypes.c_int, [_H, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                           ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
     "gemm_bf16_device_status": (ctypes.c_int, [_H, ctypes.POINTER(ctypes.c_uint32)]),
     "gemm_bf16_run_noalloc": (ctypes.c_int, [ctypes.c_int64] * 6 + [ctypes.c_void_p] * 4
                               + [ctypes.POINTER(ctypes.c_uint32)]),
@@ -161,6 +164,13 @@ def gemm_bf16_plan_info(h):
 def gemm_bf16_run(h, A: int, B: int, D: int, stream: int = 0) -> int:
     return load().gemm_bf16_run(h, ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(D),
                                 ctypes.c_void_p(stream))
+
+
+def gemm_bf16_run_fused(h, A: int, B: int, D: int, C: int, ldc: int, bias: int, alpha: float, beta: float,
+                        stream: int = 0) -> int:
+    return load().gemm_bf16_run_fused(h, ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(D),
+                                      ctypes.c_void_p(C), int(ldc), ctypes.c_void_p(bias),
+                                      float(alpha), float(beta), ctypes.c_void_p(stream))
 
 
 def gemm_bf16_run_host(h, hA, hB, hD, dA, dB, dD, stream: int = 0) -> int:
@@ -266,6 +276,23 @@ class Gemm:
             raise ValueError("run() takes device tensors; use run_host() for host operands")
         _check(gemm_bf16_run(self.h, A.data_ptr(), B.data_ptr(), D.data_ptr(), _stream_handle(stream)),
                "gemm_bf16_run")
+
+    def run_fused(self, A, B, D, C=None, bias=None, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+        """D = alpha * A @ B.T + beta * C + bias (C: M x ldc bf16 or None; bias: N bf16 or None)."""
+        import torch
+        self._validate(A, B, D)
+        M, N = self.shape[0], self.shape[1]
+        ldc = 0
+        if C is not None:
+            if C.dtype != torch.bfloat16 or not C.is_cuda:
+                raise TypeError("C must be a bf16 device tensor")
+            ldc = _ld(C, M, "C")
+        if bias is not None and (bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.numel() < N):
+            raise TypeError("bias must be a bf16 device tensor with N values")
+        _check(gemm_bf16_run_fused(self.h, A.data_ptr(), B.data_ptr(), D.data_ptr(),
+                                   0 if C is None else C.data_ptr(), ldc,
+                                   0 if bias is None else bias.data_ptr(), alpha, beta,
+                                   _stream_handle(stream)), "gemm_bf16_run_fused")
 
     def run_host(self, hA, hB, hD, dA, dB, dD, stream=None) -> None:
         """Copies hA, hB to dA, dB, runs, copies the result to hD (all enqueued on `stream`)."""

@@ -481,7 +481,18 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     return GEMM_BF16_OK;
 }
 
-GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, void *D, void *stream)
+}  // extern "C"
+
+namespace {
+
+struct FusedArgs {
+    const void *C;
+    int64_t ldc;
+    const void *bias;
+    float alpha, beta;
+};
+
+int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedArgs *fz, void *stream)
 {
     if (!h || !A || !B || !D)
         return GEMM_BF16_ERR_INVALID_ARG;
@@ -550,6 +561,30 @@ GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, voi
     if (++h->epoch == 0)
         h->epoch = 1;
     prm.epoch = h->epoch;
+    prm.C = nullptr;
+    prm.bias = nullptr;
+    prm.ldc = 0;
+    prm.alpha = 1.f;
+    prm.beta = 0.f;
+    prm.fused = 0;
+    if (fz) {
+        prm.fused = kFusedOn;
+        prm.alpha = fz->alpha;
+        prm.beta = fz->beta;
+        if (fz->C) {
+            prm.C = fz->C;
+            prm.ldc = fz->ldc;
+            prm.fused |= kFusedC;
+            if ((reinterpret_cast<uintptr_t>(fz->C) & 15u) == 0 && fz->ldc % 8 == 0)
+                prm.fused |= kFusedCVec;
+        }
+        if (fz->bias) {
+            prm.bias = fz->bias;
+            prm.fused |= kFusedBias;
+            if ((reinterpret_cast<uintptr_t>(fz->bias) & 15u) == 0)
+                prm.fused |= kFusedBiasVec;
+        }
+    }
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -581,6 +616,30 @@ GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, voi
     }
     h->last_stream = static_cast<cudaStream_t>(stream);
     return GEMM_BF16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, void *D, void *stream)
+{
+    return run_impl(h, A, B, D, nullptr, stream);
+}
+
+GEMM_BF16_API int gemm_bf16_run_fused(gemm_bf16_t h, const void *A, const void *B, void *D, const void *C,
+                                      int64_t ldc, const void *bias, float alpha, float beta, void *stream)
+{
+    if (!h)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (!h->plan.valid)
+        return GEMM_BF16_ERR_NOT_PLANNED;
+    if (C && (ldc < h->plan.N || ldc > (int64_t(1) << 38)))
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if ((C && (reinterpret_cast<uintptr_t>(C) & 1u)) || (bias && (reinterpret_cast<uintptr_t>(bias) & 1u)))
+        return GEMM_BF16_ERR_ALIGNMENT;
+    const FusedArgs fz = {C, C ? ldc : 0, bias, alpha, beta};
+    return run_impl(h, A, B, D, &fz, stream);
 }
 
 GEMM_BF16_API int gemm_bf16_run_host(gemm_bf16_t h, const void *hA, const void *hB, void *hD, void *dA, void *dB,

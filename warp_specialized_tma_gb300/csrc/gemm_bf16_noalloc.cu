@@ -210,6 +210,12 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     prm.sk_units = 0;
     prm.workspace = nullptr;
     prm.flags = nullptr;
+    prm.C = nullptr;
+    prm.bias = nullptr;
+    prm.ldc = 0;
+    prm.alpha = 1.f;
+    prm.beta = 0.f;
+    prm.fused = 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the status word must start at zero for this call (the array keeps the

@@ -150,6 +150,63 @@ __device__ __forceinline__ void epilogue_store_chunk(const uint32_t (&v0)[32], c
     }
 }
 
+// ----------------------------------------------------------------- fused epilogue
+__device__ __forceinline__ void unpack_bf16x8(const uint4 q, float (&f)[8])
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// v <- alpha * v + (beta * C[row][col] + bias[col]) in fp32 for this thread's
+// row and the chunk's 64 columns x .. x+63 (v0: x .. x+31, v1: x+32 .. x+63).
+// Columns >= N and rows >= M load nothing (their values are never stored).
+// Each element of C is read by the thread that later writes the same element
+// of D, so C may alias D.
+__device__ __forceinline__ void epilogue_fused(uint32_t (&v0)[32], uint32_t (&v1)[32], int32_t x, int32_t row,
+                                               const GemmParams &p)
+{
+    const bool has_c = (p.fused & kFusedC) && row < p.M;
+    const bool has_b = (p.fused & kFusedBias) != 0;
+    const uint16_t *crow = has_c ? static_cast<const uint16_t *>(p.C) + (int64_t)row * p.ldc : nullptr;
+    const uint16_t *bias = static_cast<const uint16_t *>(p.bias);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const int32_t col = x + 8 * g;
+        uint32_t *v = g < 4 ? &v0[8 * g] : &v1[8 * (g - 4)];
+        float cv[8], bv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            cv[i] = bv[i] = 0.f;
+        if (has_c) {
+            if ((p.fused & kFusedCVec) && col + 8 <= p.N) {
+                unpack_bf16x8(*reinterpret_cast<const uint4 *>(crow + col), cv);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (col + i < p.N)
+                        cv[i] = __uint_as_float((uint32_t)crow[col + i] << 16);
+            }
+        }
+        if (has_b) {
+            if ((p.fused & kFusedBiasVec) && col + 8 <= p.N) {
+                unpack_bf16x8(__ldg(reinterpret_cast<const uint4 *>(bias + col)), bv);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (col + i < p.N)
+                        bv[i] = __uint_as_float((uint32_t)bias[col + i] << 16);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            v[i] = __float_as_uint(fmaf(p.alpha, __uint_as_float(v[i]), fmaf(p.beta, cv[i], bv[i])));
+    }
+}
+
 // ----------------------------------------------------------------- stream-K partials
 // A CTA's fp32 partial accumulator (128 rows x 256 columns) in its workspace
 // slot, laid out as the epilogue holds it: for warp ew, chunk c, the 64 values

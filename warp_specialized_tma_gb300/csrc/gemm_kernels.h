@@ -48,6 +48,20 @@ struct GemmParams {
     int64_t sk_units;       // sk_tiles * num_k_blocks
     float *workspace;       // partials: per (cluster, rank) 128 x 256 fp32 = kPartialFloats
     uint32_t *flags;        // per (cluster, rank): == epoch once that partial is complete
+    // fused epilogue D = alpha * acc + beta * C + bias (when fused != 0)
+    const void *C;          // bf16, row pitch ldc (may alias D with ldc == ldd)
+    const void *bias;       // bf16 [N]
+    int64_t ldc;
+    float alpha, beta;
+    uint32_t fused;         // kFused* bits; 0 = plain store of the accumulator
+};
+
+enum : uint32_t {
+    kFusedOn = 1u,          // apply alpha (and beta*C, bias when present)
+    kFusedC = 2u,           // C present
+    kFusedBias = 4u,        // bias present
+    kFusedCVec = 8u,        // C rows 16-byte aligned: vector loads
+    kFusedBiasVec = 16u     // bias 16-byte aligned: vector loads
 };
 
 constexpr int kPartialFloats = kBlockM * kBlockN;  // one CTA's accumulator slice

@@ -158,6 +158,8 @@ __global__ void __launch_bounds__(kNowsThreads, 1)
                 tmem_load_wait();
                 reg_fence(v0);
                 reg_fence(v1);
+                if (p.fused)
+                    epilogue_fused(v0, v1, yb + c * 64, y + lane, p);
                 epilogue_store_chunk(v0, v1, staging, lane, p.epi_tma != 0, &tmD, yb + c * 64, y, p);
             }
             if (lane == 0)

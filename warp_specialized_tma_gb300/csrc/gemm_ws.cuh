@@ -344,6 +344,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         partial_add(p.workspace + (size_t)slot2 * kPartialFloats, ew, c, lane, v0, v1);
                     }
                 }
+                if (p.fused)
+                    epilogue_fused(v0, v1, x0 + c * 64, y + lane, p);
                 epilogue_store_chunk(v0, v1, staging, lane, tma_store, &tmD, x0 + c * 64, y, p);
             }
             if (contributor) {
