@@ -113,11 +113,23 @@ typedef enum gemm_bf16_option {
                                         partial in a handle-owned workspace (128 KiB per CTA,
                                         allocated by plan) that the owner of the tile's first
                                         k-block adds before storing; 0: every tile runs whole */
-    GEMM_BF16_OPT_PDL = 14            /* 1 (default): launch with programmatic stream serialization,
+    GEMM_BF16_OPT_PDL = 14,           /* 1 (default): launch with programmatic stream serialization,
                                         so the kernel's prologue (barrier set-up, tensor-memory
                                         allocation) overlaps the previous kernel on the stream; every
                                         global access waits for that kernel (griddepcontrol.wait).
                                         0: plain stream order */
+    GEMM_BF16_OPT_EPI_SCHEDULE = 15,  /* WS kernel's epilogue warpgroups.  0 (default) = cooperative:
+                                        both warpgroups drain every tile (a warp: 32 rows x 128
+                                        columns).  1 = ping-pong: warpgroup g drains the tiles of
+                                        tensor-memory accumulator g, i.e. every other tile (a warp:
+                                        32 rows x 256 columns); needs ACC_BUFFERS = 2, else plan
+                                        fails with INVALID_ARG */
+    GEMM_BF16_OPT_SCHEDULER = 16      /* WS kernel's tile order.  0 (default) = static: each SM
+                                        (pair) walks the grid-stride sequence.  1 = dynamic: after
+                                        its stream-K share, each SM (pair) takes the next whole tile
+                                        from a device counter owned by the handle, so faster SMs
+                                        take more tiles; the last SM (pair) to finish resets the
+                                        counter, so launches of one handle must not overlap */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */
@@ -142,11 +154,14 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t regs_per_thread;      /* registers per thread the kernel is launched with */
     int32_t stage_group;          /* ring stages released per commit */
     int32_t sk_tiles;             /* tiles split along k (stream-K); 0 = none */
+    int32_t epi_schedule;         /* 0 = cooperative, 1 = ping-pong */
+    int32_t scheduler;            /* 0 = static, 1 = dynamic */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's
- * current device).  Allocates the handle (host) and a 4-byte device status word
- * that the kernels' watchdog writes.  Fails with UNSUPPORTED unless the device
+ * current device).  Allocates the handle (host) and 16 bytes of device memory:
+ * the status word that the kernels' watchdog writes and the dynamic
+ * scheduler's tile counter.  Fails with UNSUPPORTED unless the device
  * is compute capability 10.3 (sm_103), with CUDA if no device is usable.
  * On success *out owns both allocations until gemm_bf16_destroy. */
 GEMM_BF16_API int gemm_bf16_create(int device, gemm_bf16_t *out);

@@ -118,6 +118,12 @@ MID = [(256, 256, 256), (300, 520, 200), (129, 257, 65), (640, 384, 1000), (1000
     dict(cta_group=1, stage_group=1),
     dict(cta_group=1, persistent=0),
     dict(cta_group=2, persistent=0),
+    dict(cta_group=1, epi_schedule=1),
+    dict(cta_group=2, epi_schedule=1),
+    dict(cta_group=1, scheduler=1),
+    dict(cta_group=2, scheduler=1),
+    dict(cta_group=2, epi_schedule=1, scheduler=1),
+    dict(cta_group=2, scheduler=1, persistent=0),
     dict(pipeline=binding.PIPE_SYNC_WAR),
     dict(pipeline=binding.PIPE_MBAR_WAR),
 ])
@@ -157,6 +163,83 @@ def test_stream_k_split_tiles_exact(cta_group, M, N, K, max_ctas):
     # the split schedule and the whole-tile schedule agree bit for bit here
     D0 = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stream_k=0)
     assert torch.equal(D.view(torch.int16), D0.view(torch.int16))
+
+
+SCHEDULES = [dict(epi_schedule=1), dict(scheduler=1), dict(epi_schedule=1, scheduler=1)]
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("sched", SCHEDULES)
+@pytest.mark.parametrize("max_ctas,K", [(2, 520), (6, 64), (10, 200)])
+def test_schedules_few_ctas_many_tiles_repeated(cta_group, sched, max_ctas, K):
+    # Many items per SM (pair): the schedule ring and both epilogue groups wrap
+    # many times; K = 64 gives one k-block per tile, so the producer runs
+    # several tiles ahead.  Four launches on one handle: the dynamic counter
+    # must be back at 0 before each.
+    M, N = 1100, 1300
+    A, B = inputs.make_problem(M, N, K, "int2", seed=23 + K)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    outs = []
+    with binding.Gemm(0, cta_group=cta_group, max_ctas=max_ctas, **sched) as g:
+        info = g.plan(M, N, K)
+        assert info["epi_schedule"] == sched.get("epi_schedule", 0)
+        assert info["scheduler"] == sched.get("scheduler", 0)
+        for _ in range(4):
+            D = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=dev)
+            g.run(dA, dB, D)
+            outs.append(D)
+        st, detail = g.device_status()
+        assert st == binding.OK, f"device status {st} detail {detail:#x}"
+    torch.cuda.synchronize()
+    check(outs[0].cpu(), A, B, M, N, K, exact=True)
+    for D in outs[1:]:
+        assert torch.equal(D.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("sched", SCHEDULES)
+def test_schedules_with_stream_k_split_tiles(cta_group, sched):
+    M, N, K, max_ctas = 2048, 1536, 2560, 10
+    A, B = inputs.make_problem(M, N, K, "int2", seed=M + K)
+    with binding.Gemm(0, cta_group=cta_group, max_ctas=max_ctas, **sched) as g:
+        assert g.plan(M, N, K)["sk_tiles"] > 0
+    D = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, **sched)
+    check(D, A, B, M, N, K, exact=True)
+    D0 = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas)
+    assert torch.equal(D.view(torch.int16), D0.view(torch.int16))
+
+
+def test_schedule_options_are_validated():
+    with binding.Gemm(0, epi_schedule=1, acc_buffers=1) as g:
+        with pytest.raises(binding.GemmError) as e:
+            g.plan(512, 512, 512)
+        assert e.value.status == binding.ERR_INVALID_ARG
+    with binding.Gemm(0, epi_schedule=1, scheduler=1, pipeline=binding.PIPE_MBAR_WAR) as g:
+        info = g.plan(512, 512, 512)  # the ablation loops have neither schedule
+        assert info["epi_schedule"] == 0 and info["scheduler"] == 0
+
+
+def test_dynamic_scheduler_recovers_after_watchdog_timeout():
+    # a load is skipped, the launch gives up part-way with tiles left in the
+    # counter; the next launch on the same handle must still cover every tile
+    M, N, K = 1024, 1024, 1024
+    A, B = inputs.make_problem(M, N, K, "int2", seed=31)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0, watchdog_ns=20_000_000, fault_skip_load=5, scheduler=1, max_ctas=4) as g:
+        g.plan(M, N, K)
+        g.run(dA, dB, dD)
+        st, detail = g.device_status()
+        assert st == binding.ERR_DEVICE_TIMEOUT and detail & 0x80000000
+        g.set_option("fault_skip_load", -1)
+        g.plan(M, N, K)
+        for _ in range(2):
+            dD.fill_(3.0)
+            g.run(dA, dB, dD)
+            assert g.device_status()[0] == binding.OK
+            check(dD.cpu(), A, B, M, N, K, exact=True)
 
 
 def test_stream_k_random_inputs_and_repeated_launches():
@@ -394,6 +477,7 @@ def run_fused_gpu(A, B, M, N, K, C=None, bias=None, alpha=1.0, beta=0.0, ldd=Non
 
 
 @pytest.mark.parametrize("variant", [dict(), dict(cta_group=1), dict(max_ctas=14),
+                                     dict(max_ctas=14, epi_schedule=1, scheduler=1),
                                      dict(pipeline=binding.PIPE_MBAR_WAR), dict(epilogue=2)])
 def test_fused_epilogue_exact_integers(variant):
     M, N, K = 1100, 900, 2560

@@ -14,6 +14,9 @@ stage ring with __syncthreads up to the default kernel:
   +2cta       an SM pair per 256x256 tile (cta_group::2)
   +streamk    the partial last wave of tiles split along k (the default)
 
+With --schedules the default kernel is compared with its schedule options
+instead: the ping-pong epilogue, the dynamic tile counter, and both.
+
 Rungs run interleaved in shuffled order for several rounds (the GPU's power
 limit moves the clock between runs) and the best and median times are printed
 as one JSON line per rung.
@@ -43,12 +46,21 @@ RUNGS = [
 ]
 
 
+SCHEDULE_RUNGS = [
+    ("default", dict()),
+    ("pingpong", dict(epi_schedule=1)),
+    ("dynamic", dict(scheduler=1)),
+    ("pingpong+dynamic", dict(epi_schedule=1, scheduler=1)),
+]
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--workload", default="cube8192", choices=list(inputs.WORKLOADS))
     ap.add_argument("--rounds", type=int, default=5)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--device", type=int, default=0)
+    ap.add_argument("--schedules", action="store_true", help="compare the schedule options")
     args = ap.parse_args(argv)
 
     libbuild.build()
@@ -60,7 +72,7 @@ def main(argv=None) -> int:
     dA, dB = A.to(dev), B.to(dev)
     dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     handles = []
-    for name, opts in RUNGS:
+    for name, opts in (SCHEDULE_RUNGS if args.schedules else RUNGS):
         g = binding.Gemm(args.device, **opts)
         handles.append((name, g, g.plan(M, N, K)))
 

@@ -46,6 +46,8 @@ OPTIONS = {
     "stage_group": 12,
     "stream_k": 13,
     "pdl": 14,
+    "epi_schedule": 15,
+    "scheduler": 16,
 }
 
 # the C entry points and their signatures
@@ -93,6 +95,8 @@ class PlanInfo(ctypes.Structure):
         ("regs_per_thread", ctypes.c_int32),
         ("stage_group", ctypes.c_int32),
         ("sk_tiles", ctypes.c_int32),
+        ("epi_schedule", ctypes.c_int32),
+        ("scheduler", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

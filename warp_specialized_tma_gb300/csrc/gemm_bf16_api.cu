@@ -20,7 +20,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 15;
+constexpr int kNumOptions = 17;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 
 struct Plan {
@@ -36,6 +36,8 @@ struct Plan {
     int stages = 0;
     int raster_group = 8;
     int epilogue_opt = 0;
+    int epi_pingpong = 0;
+    int sched_dynamic = 0;
     int64_t tiles = 0;
     int num_m_blocks = 0, num_n_blocks = 0, num_k_blocks = 0;
     int grid_ctas = 0;
@@ -54,6 +56,8 @@ struct gemm_bf16 {
     int device = 0;
     int num_sms = 0;
     size_t max_smem_optin = 0;
+    // device words: [0] watchdog status, [1] unused, [2] dynamic scheduler's next
+    // whole tile, [3] clusters finished (both 0 between launches)
     uint32_t *d_err = nullptr;
     int64_t opt[kNumOptions];
     Plan plan;
@@ -90,6 +94,8 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_STAGE_GROUP: return 0;
     case GEMM_BF16_OPT_STREAM_K: return 1;
     case GEMM_BF16_OPT_PDL: return 1;
+    case GEMM_BF16_OPT_EPI_SCHEDULE: return 0;
+    case GEMM_BF16_OPT_SCHEDULER: return 0;
     default: return 0;
     }
 }
@@ -111,6 +117,8 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_STAGE_GROUP: return v >= 0 && v <= 2;
     case GEMM_BF16_OPT_STREAM_K: return v == 0 || v == 1;
     case GEMM_BF16_OPT_PDL: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_EPI_SCHEDULE: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_SCHEDULER: return v == 0 || v == 1;
     default: return false;
     }
 }
@@ -243,8 +251,8 @@ GEMM_BF16_API int gemm_bf16_create(int device, gemm_bf16_t *out)
     h->max_smem_optin = (size_t)optin;
     for (int k = 0; k < kNumOptions; ++k)
         h->opt[k] = default_option(k);
-    if (cudaMalloc(&h->d_err, sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
+    if (cudaMalloc(&h->d_err, 4 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) {
         cudaGetLastError();
         if (h->d_err)
             cudaFree(h->d_err);
@@ -307,6 +315,8 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
     pl.setmaxnreg = (int)h->opt[GEMM_BF16_OPT_SETMAXNREG];
     pl.raster_group = (int)h->opt[GEMM_BF16_OPT_RASTER_GROUP];
     pl.epilogue_opt = (int)h->opt[GEMM_BF16_OPT_EPILOGUE];
+    pl.epi_pingpong = (int)h->opt[GEMM_BF16_OPT_EPI_SCHEDULE];
+    pl.sched_dynamic = (int)h->opt[GEMM_BF16_OPT_SCHEDULER];
     pl.fault_skip = (int)h->opt[GEMM_BF16_OPT_FAULT_SKIP_LOAD];
     pl.watchdog_ns = (uint64_t)h->opt[GEMM_BF16_OPT_WATCHDOG_NS];
     pl.epi_tma_allowed = ((ldd * 2) % 16) == 0;
@@ -320,10 +330,14 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         pl.persistent = 0;
         pl.acc_buffers = 1;
         pl.setmaxnreg = 0;
+        pl.epi_pingpong = 0;
+        pl.sched_dynamic = 0;
     } else if (cg == 0) {
         cg = 2;  // an SM pair per 256x256 tile halves each SM's operand traffic
     }
     pl.cta_group = cg;
+    if (pl.epi_pingpong && pl.acc_buffers != 2)
+        return GEMM_BF16_ERR_INVALID_ARG;  // each epilogue warpgroup owns one accumulator
 
     pl.num_m_blocks = (int)((M + (int64_t)kBlockM * cg - 1) / ((int64_t)kBlockM * cg));
     pl.num_n_blocks = (int)((N + kBlockN - 1) / kBlockN);
@@ -478,6 +492,8 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->epilogue_tma_allowed = p.epi_tma_allowed ? 1 : 0;
     info->raster_group = p.raster_group;
     info->regs_per_thread = p.regs;
+    info->epi_schedule = p.epi_pingpong;
+    info->scheduler = p.sched_dynamic;
     return GEMM_BF16_OK;
 }
 
@@ -567,6 +583,9 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     prm.alpha = 1.f;
     prm.beta = 0.f;
     prm.fused = 0;
+    prm.epi_pingpong = pl.epi_pingpong;
+    prm.sched_dynamic = pl.sched_dynamic;
+    prm.sched = h->d_err + 2;
     if (fz) {
         prm.fused = kFusedOn;
         prm.alpha = fz->alpha;
@@ -683,8 +702,11 @@ GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail)
         return GEMM_BF16_ERR_CUDA;
     }
     uint32_t w = 0;
+    // Clearing the whole block also puts the tile counter back to 0: after a
+    // watchdog give-up it is the only thing that does (normally the last SM
+    // pair of each launch resets it).
     if (cudaMemcpy(&w, h->d_err, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess ||
+        (w != 0 && cudaMemset(h->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;

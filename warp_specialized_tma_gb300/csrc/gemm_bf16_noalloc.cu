@@ -216,6 +216,9 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     prm.alpha = 1.f;
     prm.beta = 0.f;
     prm.fused = 0;
+    prm.epi_pingpong = 0;
+    prm.sched_dynamic = 0;  // the counter lives in a handle
+    prm.sched = nullptr;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the status word must start at zero for this call (the array keeps the

@@ -280,4 +280,55 @@ __device__ __forceinline__ bool warp_wait(const WaitCtl &ctl, uint32_t bar, uint
     return ok != 0;
 }
 
+// ----------------------------------------------------------------- schedule ring
+// With the dynamic scheduler the leader CTA's producer decides the work
+// sequence (its stream-K share, then whole tiles taken from a global counter)
+// and publishes item `seq` in slot seq % kRingSlots of every CTA of the
+// cluster.  Each slot has a "full" barrier (count 1, in every CTA) and an
+// "empty" barrier on the leader that collects one arrival from each reader:
+// the MMA issuer, one epilogue thread per CTA and the peer's producer.  A tile
+// of -1 ends the sequence.
+
+// Publisher: wait until the slot's previous item has been read by every
+// reader, write the item into this CTA's slot and the peer's, arrive on both
+// full barriers.
+template <bool kCluster>
+__device__ __forceinline__ bool ring_put(const WaitCtl &ctl, uint32_t ring, uint32_t ring_full, uint32_t ring_empty,
+                                         uint32_t peer_ring, uint32_t peer_full, int32_t seq, const WorkItem &w)
+{
+    const uint32_t r = (uint32_t)seq & (uint32_t)(kRingSlots - 1);
+    const uint32_t ph = ((uint32_t)seq / (uint32_t)kRingSlots) & 1u;
+    if (!ctl.wait<kCluster>(ring_empty + 8u * r, ph ^ 1u, kRoleSched, 0x800u | r))
+        return false;
+    st_shared_v4(ring + 16u * r, (uint32_t)w.tile, (uint32_t)w.kb0, (uint32_t)w.kb1, 0u);
+    mbar_arrive(ring_full + 8u * r);
+    if constexpr (kCluster) {
+        st_shared_cluster_v4(peer_ring + 16u * r, (uint32_t)w.tile, (uint32_t)w.kb0, (uint32_t)w.kb1, 0u);
+        mbar_arrive_cluster(peer_full + 8u * r);  // release.cluster: the item is visible first
+    }
+    return true;
+}
+
+// Reader: wait for item `seq`, copy it, release the slot on the leader's empty
+// barrier (`leader_empty` is a shared::cluster address in 2-CTA mode).
+template <bool kCluster>
+__device__ __forceinline__ bool ring_get(const WaitCtl &ctl, uint32_t ring, uint32_t ring_full, uint32_t leader_empty,
+                                         int32_t seq, WorkItem &w)
+{
+    const uint32_t r = (uint32_t)seq & (uint32_t)(kRingSlots - 1);
+    const uint32_t ph = ((uint32_t)seq / (uint32_t)kRingSlots) & 1u;
+    if (!ctl.wait<kCluster>(ring_full + 8u * r, ph, kRoleSched, r))
+        return false;
+    uint32_t a, b, c, d;
+    ld_shared_v4(ring + 16u * r, a, b, c, d);
+    w.tile = (int32_t)a;
+    w.kb0 = (int32_t)b;
+    w.kb1 = (int32_t)c;
+    if constexpr (kCluster)
+        mbar_arrive_cluster(leader_empty + 8u * r);
+    else
+        mbar_arrive(leader_empty + 8u * r);
+    return true;
+}
+
 }  // namespace wstma

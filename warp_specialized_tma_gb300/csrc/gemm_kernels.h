@@ -20,6 +20,7 @@ constexpr int kWsThreads = 384;   // WG0: producer / MMA / TMEM-alloc / spare wa
 constexpr int kNowsThreads = 128; // the non-specialised ablation kernels
 constexpr int kStagingBytes = 32 * 64 * 2;  // per-warp epilogue staging: 32 rows x 64 bf16
 constexpr int kMaxStages = 8;
+constexpr int kRingSlots = 8;     // schedule ring depth (power of two)
 
 // Producer / consumer register budgets for setmaxnreg (whole warpgroups).
 constexpr int kProducerRegs = 56;
@@ -54,6 +55,10 @@ struct GemmParams {
     int64_t ldc;
     float alpha, beta;
     uint32_t fused;         // kFused* bits; 0 = plain store of the accumulator
+    // schedules (WS only)
+    int32_t epi_pingpong;   // 1 = epilogue warpgroup g drains the tiles of accumulator g
+    int32_t sched_dynamic;  // 1 = whole tiles are taken from the counter sched[0]
+    uint32_t *sched;        // [0] next whole tile, [1] clusters finished; both 0 between launches
 };
 
 enum : uint32_t {
@@ -71,7 +76,7 @@ inline size_t ws_smem_bytes(int cta_group, int stages)
 {
     const size_t stage = (size_t)kBlockM * kBlockK * 2 + (size_t)(kBlockN / cta_group) * kBlockK * 2;
     return 1024 /* alignment slack */ + (size_t)stages * stage + (size_t)kEpiWarps * kStagingBytes +
-           256 /* barriers, tmem slot, abort flag */;
+           512 /* schedule ring, barriers, tmem slot, abort flag, epilogue go words */;
 }
 
 inline size_t nows_smem_bytes(int stages)

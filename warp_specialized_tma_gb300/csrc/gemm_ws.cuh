@@ -2,7 +2,8 @@
 // accumulation in tensor memory, bf16 out.
 //
 // Roles (384 threads, one CTA per SM):
-//   warpgroup 0: warp 0 lane 0  = TMA producer
+//   warpgroup 0: warp 0 lane 0  = TMA producer (and, with the dynamic scheduler,
+//                                 the leader's publisher of the work sequence)
 //                warp 1 lane 0  = tcgen05 MMA issuer (leader CTA only in 2-CTA mode)
 //                warp 2         = tensor-memory allocator
 //                warp 3         = spare
@@ -23,6 +24,15 @@
 // cutlass PR #3316 ("Fix race condition in 2SM TMEM alloc ...") gives the
 // 2-CTA rule: both CTAs pass a cluster barrier before the paired
 // tcgen05.alloc.
+//
+// Two schedule options (runtime switches in GemmParams):
+//   epilogue  cooperative (default): both epilogue warpgroups drain every tile;
+//             ping-pong: warpgroup g drains the tiles of accumulator g, so the
+//             two groups alternate tiles (Fuser #3941's second consumer
+//             schedule, with TMEM accumulators instead of register ones).
+//   tiles     static (default): every role walks the same grid-stride sequence;
+//             dynamic: the leader's producer takes whole tiles from a global
+//             counter and publishes them through the schedule ring.
 #pragma once
 
 #include "gemm_common.cuh"
@@ -53,19 +63,24 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t g_mask = p.stage_group == 2 ? 1u : 0u;
     const uint32_t stage0 = base;
     const uint32_t staging0 = base + (uint32_t)S * kStageBytes;
-    const uint32_t full_bar = staging0 + kEpiWarps * kStagingBytes;
+    const uint32_t ring = staging0 + kEpiWarps * kStagingBytes;  // kRingSlots x 16 B work items
+    const uint32_t full_bar = ring + 16u * kRingSlots;
     const uint32_t empty_bar = full_bar + 8u * S;
     const uint32_t accf_bar = empty_bar + 8u * S;
     const uint32_t acce_bar = accf_bar + 16u;
     const uint32_t done_bar = acce_bar + 16u;
-    const uint32_t tmem_slot = done_bar + 8u;
+    const uint32_t ring_full = done_bar + 8u;
+    const uint32_t ring_empty = ring_full + 8u * kRingSlots;
+    const uint32_t tmem_slot = ring_empty + 8u * kRingSlots;
     const uint32_t abort_flag = tmem_slot + 4u;
-    const uint32_t go_flags = abort_flag + 4u;  // two words, see the epilogue
+    const uint32_t go_area = abort_flag + 4u;  // 2 groups x 2 parities x 4 words, see the epilogue
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = kCluster ? cluster_ctarank() : 0u;
     const uint32_t acc_cols = (uint32_t)kBlockN * (uint32_t)p.acc_buffers;  // 256 or 512
+    const bool pingpong = p.epi_pingpong != 0;
+    const bool dyn = p.sched_dynamic != 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -74,9 +89,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(accf_bar + 8u * a, 1);
-            mbar_init(acce_bar + 8u * a, kEpiWarps * CG);
+            // every warp of the warpgroup(s) that drain accumulator a, in both CTAs
+            mbar_init(acce_bar + 8u * a, (pingpong ? kEpiWarps / 2 : kEpiWarps) * CG);
         }
         mbar_init(done_bar, 1);
+        for (int r = 0; r < kRingSlots; ++r) {
+            mbar_init(ring_full + 8u * r, 1);
+            mbar_init(ring_empty + 8u * r, 2 * CG);  // MMA issuer, CG epilogue pollers, CG-1 peer producers
+        }
         st_shared_u32(abort_flag, 0u);
         fence_mbarrier_init();
     }
@@ -101,8 +121,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
     // Everything above touched only this CTA's shared and tensor memory, so it
-    // may overlap the previous kernel on the stream; from here on A, B, D and
-    // the workspace are read or written.
+    // may overlap the previous kernel on the stream; from here on A, B, D, the
+    // workspace and the tile counter are read or written.
     grid_dependency_wait();
 
     WaitCtl ctl;
@@ -113,6 +133,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 
     const int32_t cluster_id = (int32_t)blockIdx.x / CG;
     const int32_t num_clusters = (int32_t)gridDim.x / CG;
+    const int32_t KB = p.num_k_blocks;
+    // readers release ring slots on the leader's empty barriers
+    const uint32_t leader_ring_empty = kCluster ? mapa_shared(ring_empty, 0u) : ring_empty;
 
     if (warp < 4) {
         if constexpr (kSetMaxNReg)
@@ -125,14 +148,56 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (warp == 0 && lane == 0) {
             // ---------------- TMA producer: one loop over (tile, k-block) ----------------
             const uint32_t full_target = kCluster ? mapa_shared(full_bar, 0u) : full_bar;
+            const bool publisher = dyn && rank == 0;
+            const uint32_t peer_ring = kCluster ? mapa_shared(ring, 1u) : 0u;
+            const uint32_t peer_ring_full = kCluster ? mapa_shared(ring_full, 1u) : 0u;
             int s = 0;
             uint32_t ph = 0;
             int32_t it = 0;
+            int32_t seq = 0;
             bool ok = true;
+            bool counter_done = false;
             WorkIter wi;
             wi.init(p, cluster_id, num_clusters);
+            if (dyn)
+                wi.dp = wi.T;  // whole tiles come from the counter, not from the grid stride
             WorkItem w;
-            while (ok && wi.next(w)) {
+            for (;;) {
+                bool have;
+                if (!dyn) {
+                    have = wi.next(w);
+                } else if (publisher) {
+                    // this cluster's stream-K share first, then whole tiles on demand
+                    have = wi.next(w);
+                    if (!have && !counter_done) {
+                        const int32_t t = p.sk_tiles + (int32_t)atomicAdd(p.sched, 1u);
+                        if (t < p.num_tiles) {
+                            w.tile = t;
+                            w.kb0 = 0;
+                            w.kb1 = KB;
+                            have = true;
+                        } else {
+                            counter_done = true;
+                        }
+                    }
+                    WorkItem out = w;
+                    if (!have)
+                        out.tile = -1;
+                    if (!ring_put<kCluster>(ctl, ring, ring_full, ring_empty, peer_ring, peer_ring_full, seq, out)) {
+                        ok = false;
+                        break;
+                    }
+                    ++seq;
+                } else {
+                    if (!ring_get<kCluster>(ctl, ring, ring_full, leader_ring_empty, seq, w)) {
+                        ok = false;
+                        break;
+                    }
+                    ++seq;
+                    have = w.tile >= 0;
+                }
+                if (!have)
+                    break;
                 const TileCoord tc = tile_coord(w.tile, p);
                 const int32_t ya = tc.mb * kTileM + (int32_t)rank * kBlockM;
                 const int32_t yb = tc.nb * kBlockN + (int32_t)rank * (int32_t)kBRows;
@@ -165,6 +230,24 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         ph ^= 1u;
                     }
                 }
+                if (!ok)
+                    break;
+            }
+            if (publisher) {
+                // A second end marker: ping-pong epilogue groups read alternate slots.
+                if (ok) {
+                    WorkItem end = {-1, 0, 0};
+                    ring_put<kCluster>(ctl, ring, ring_full, ring_empty, peer_ring, peer_ring_full, seq, end);
+                }
+                // This cluster takes no more tiles.  The last cluster to get here
+                // (every other one has made its last counter access) puts the
+                // counter back to 0 for the next launch.
+                __threadfence();
+                if (atomicAdd(p.sched + 1, 1u) == (uint32_t)num_clusters - 1u) {
+                    atomicExch(p.sched, 0u);
+                    atomicExch(p.sched + 1, 0u);
+                    __threadfence();
+                }
             }
             // This CTA issues no more loads: the next kernel on the stream may begin
             // launching (its CTAs start as this grid's CTAs exit).
@@ -194,12 +277,24 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             uint32_t ph = 0;
             int acc = 0;
             uint32_t acc_ph = 0;
+            int32_t seq = 0;
             bool ok = true;
             bool ready = false;  // outcome of the look-ahead probe of ring slot (s, ph)
             WorkIter wi;
             wi.init(p, cluster_id, num_clusters);
             WorkItem w;
-            while (ok && wi.next(w)) {
+            for (;;) {
+                if (dyn) {
+                    if (!ring_get<kCluster>(ctl, ring, ring_full, leader_ring_empty, seq, w)) {
+                        ok = false;
+                        break;
+                    }
+                    ++seq;
+                    if (w.tile < 0)
+                        break;
+                } else if (!wi.next(w)) {
+                    break;
+                }
                 // the epilogue has drained this accumulator (one lap ago)
                 if (!ctl.wait<kCluster>(acce_bar + 8u * acc, acc_ph ^ 1u, kRoleMmaAcc, (uint32_t)acc)) {
                     ok = false;
@@ -264,38 +359,76 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             setmaxnreg_inc<kConsumerRegs>();
 
         // ---------------- epilogue: tile { TMEM -> bf16 -> D } ----------------
+        // Cooperative: both warpgroups drain every tile, a warp takes 32 rows x
+        // 128 columns.  Ping-pong: warpgroup g drains the items that use
+        // accumulator g (items g, g+2, ... of the sequence), a warp takes 32 rows
+        // x 256 columns.
         const int ew = warp - 4;        // 0..7
         const int q = warp & 3;         // tensor-memory lane quadrant this warp may read
-        const int half = ew >> 2;       // column half of the 256-wide accumulator
+        const int grp = pingpong ? (ew >> 2) : 0;
+        const uint32_t group_threads = pingpong ? 128u : (uint32_t)kEpiWarps * 32u;
+        const bool poller = pingpong ? (q == 0) : (ew == 0);
+        const int nchunks = pingpong ? 4 : 2;
+        const int32_t col0 = pingpong ? 0 : (ew >> 2) * 128;
+        const int32_t seq_step = pingpong ? 2 : 1;
         const uint32_t staging = staging0 + (uint32_t)ew * kStagingBytes;
         const uint32_t acce_target = kCluster ? mapa_shared(acce_bar, 0u) : acce_bar;
         const bool tma_store = p.epi_tma != 0;
-        int acc = 0;
+        int acc = grp;
         uint32_t acc_ph = 0;
         uint32_t tile_parity = 0;
+        int32_t seq = grp;
         WorkIter wi;
         wi.init(p, cluster_id, num_clusters);
-        WorkItem w;
-        const int32_t KB = p.num_k_blocks;
-        while (wi.next(w)) {
+        if (pingpong && grp == 1 && !dyn) {
+            WorkItem skip;
+            wi.next(skip);
+        }
+        for (;;) {
+            // One thread per group finds the next item and polls the accumulator
+            // barrier, then posts both; the other warps sleep on a named barrier
+            // instead of polling (every poll competes with the MMA issuer).  The
+            // posted words alternate with the item parity, so a warp that is one
+            // item behind never reads the next item's words.
+            const uint32_t go = go_area + 16u * (2u * (uint32_t)grp + tile_parity);
+            if (poller) {
+                WorkItem w = {0, 0, 0};
+                uint32_t st = 1;  // 1 = drain item w, 2 = no more items, 0 = gave up
+                if (lane == 0) {
+                    if (dyn) {
+                        if (!ring_get<kCluster>(ctl, ring, ring_full, leader_ring_empty, seq, w))
+                            st = 0;
+                        else if (w.tile < 0)
+                            st = 2;
+                    } else if (!wi.next(w)) {
+                        st = 2;
+                    } else if (pingpong) {
+                        WorkItem skip;  // the other group's item
+                        wi.next(skip);
+                    }
+                }
+                st = __shfl_sync(0xFFFFFFFFu, st, 0);
+                if (st == 1u &&
+                    !warp_wait<kCluster>(ctl, accf_bar + 8u * acc, acc_ph, kRoleEpilogue, (uint32_t)acc, lane))
+                    st = 0;
+                if (lane == 0) {
+                    st_volatile_shared_u32(go + 4u, (uint32_t)w.tile);
+                    st_volatile_shared_u32(go + 8u, (uint32_t)w.kb0);
+                    st_volatile_shared_u32(go + 12u, (uint32_t)w.kb1);
+                    st_volatile_shared_u32(go, st);
+                }
+            }
+            named_barrier_sync(1u + (uint32_t)grp, group_threads);
+            if (ld_volatile_shared_u32(go) != 1u)
+                break;
+            WorkItem w;
+            w.tile = (int32_t)ld_volatile_shared_u32(go + 4u);
+            w.kb0 = (int32_t)ld_volatile_shared_u32(go + 8u);
+            w.kb1 = (int32_t)ld_volatile_shared_u32(go + 12u);
+            seq += seq_step;
+            tc_fence_after_sync();
             const TileCoord tc = tile_coord(w.tile, p);
             const int32_t y = tc.mb * kTileM + (int32_t)rank * kBlockM + q * 32;
-            const int32_t x0 = tc.nb * kBlockN + half * 128;
-            // One thread polls the accumulator barrier and posts the outcome; the
-            // other epilogue warps sleep on a named barrier instead of polling
-            // (every poll competes with the MMA issuer).  The outcome word
-            // alternates with the tile parity, so a warp that is one tile behind
-            // never reads the next tile's word.
-            const uint32_t go = go_flags + 4u * tile_parity;
-            if (ew == 0) {
-                const bool okw = warp_wait<kCluster>(ctl, accf_bar + 8u * acc, acc_ph, kRoleEpilogue, (uint32_t)acc, lane);
-                if (lane == 0)
-                    st_volatile_shared_u32(go, okw ? 1u : 0u);
-            }
-            named_barrier_sync(1, kEpiWarps * 32);
-            if (ld_volatile_shared_u32(go) == 0u)
-                break;
-            tc_fence_after_sync();
             // A stream-K item that does not start at k-block 0 is a contributor: it
             // leaves its fp32 partial for the tile's owner.  The item holding
             // k-block 0 of a split tile is the owner: it adds every contributor's
@@ -304,16 +437,21 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const bool contributor = w.kb0 > 0;
             const bool owner = w.kb0 == 0 && w.kb1 < KB;
             const int32_t slot_id = cluster_id * CG + (int32_t)rank;
-            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBlockN + half * 128);
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBlockN + col0);
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int32_t col = col0 + c * 64;  // column of the chunk inside the tile
+                // the partials keep one layout whatever the schedule: the chunk of
+                // column `col` and quadrant q belongs to (virtual) warp pw, chunk pc
+                const int pw = (col >> 7) * 4 + q;
+                const int pc = (col >> 6) & 1;
                 uint32_t v0[32], v1[32];
                 tmem_load_32x32(tbase + (uint32_t)(c * 64), v0);
                 tmem_load_32x32(tbase + (uint32_t)(c * 64 + 32), v1);
                 tmem_load_wait();
                 reg_fence(v0);
                 reg_fence(v1);
-                if (c == 1) {
+                if (c == nchunks - 1) {
                     // every read of this accumulator is done: hand it back to the MMA warp
                     tc_fence_before_sync();
                     __syncwarp();
@@ -325,7 +463,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     }
                 }
                 if (contributor) {
-                    partial_store(p.workspace + (size_t)slot_id * kPartialFloats, ew, c, lane, v0, v1);
+                    partial_store(p.workspace + (size_t)slot_id * kPartialFloats, pw, pc, lane, v0, v1);
                     continue;
                 }
                 if (owner) {
@@ -341,21 +479,24 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         const int32_t slot2 = c2 * CG + (int32_t)rank;
                         if (c == 0 && !warp_wait_flag(ctl, p.flags + slot2, p.epoch, lane))
                             break;
-                        partial_add(p.workspace + (size_t)slot2 * kPartialFloats, ew, c, lane, v0, v1);
+                        partial_add(p.workspace + (size_t)slot2 * kPartialFloats, pw, pc, lane, v0, v1);
                     }
                 }
+                const int32_t x = tc.nb * kBlockN + col;
                 if (p.fused)
-                    epilogue_fused(v0, v1, x0 + c * 64, y + lane, p);
-                epilogue_store_chunk(v0, v1, staging, lane, tma_store, &tmD, x0 + c * 64, y, p);
+                    epilogue_fused(v0, v1, x, y + lane, p);
+                epilogue_store_chunk(v0, v1, staging, lane, tma_store, &tmD, x, y, p);
             }
             if (contributor) {
                 // publish the partial: every writer fences, then one thread raises the flag
                 __threadfence();
-                named_barrier_sync(2, kEpiWarps * 32);
-                if (ew == 0 && lane == 0)
+                named_barrier_sync(3u + (uint32_t)grp, group_threads);
+                if (poller && lane == 0)
                     st_release_gpu_u32(p.flags + slot_id, p.epoch);
             }
-            if (p.acc_buffers == 2) {
+            if (pingpong) {
+                acc_ph ^= 1u;
+            } else if (p.acc_buffers == 2) {
                 acc ^= 1;
                 if (acc == 0)
                     acc_ph ^= 1u;

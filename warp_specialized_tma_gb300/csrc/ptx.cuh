@@ -62,6 +62,17 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d)
+{
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Store to a (possibly peer CTA's) shared::cluster address.
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
 {
@@ -216,7 +227,8 @@ enum : uint32_t {
     kRoleEpilogue = 4,   // epilogue waiting for a finished accumulator
     kRoleDrain = 5,      // teardown waiting for copies / MMAs in flight
     kRoleNoWs = 6,       // non-specialised ablation kernels
-    kRoleFixup = 7       // stream-K owner waiting for a contributor's partial
+    kRoleFixup = 7,      // stream-K owner waiting for a contributor's partial
+    kRoleSched = 8       // schedule ring: waiting for an item, or for a free slot
 };
 
 // ---------------------------------------------------------------- global flags
