@@ -350,6 +350,27 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e2e_ms = dist.max(e0.elapsed_time(e1), dev)
     e2e_value = aggregate(flops, args.e2e_steps, e2e_ms, world)
+
+    # The same host <-> device copies with no GEMM, scheduled the same way: the
+    # host link's bound on the end-to-end rate (a link measurement, no kernel).
+    torch.cuda.synchronize(dev)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    c0.record(streams[0])
+    streams[1].wait_event(c0)
+    for i in range(args.e2e_steps):
+        j = i % 2
+        with torch.cuda.stream(streams[j]):
+            bufs[j][0].copy_(hA, non_blocking=True)
+            bufs[j][1].copy_(hB, non_blocking=True)
+            hDs[j].copy_(bufs[j][2], non_blocking=True)
+    streams[0].wait_stream(streams[1])
+    c1.record(streams[0])
+    torch.cuda.synchronize(dev)
+    copy_ms = dist.max(c0.elapsed_time(c1), dev)
+    copy_bound = aggregate(flops, args.e2e_steps, copy_ms, world)
     for gg in gs:
         st, detail = gg.device_status()
         if st != binding.OK:
@@ -389,7 +410,9 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * (M * K + N * K),
                     "d2h_bytes_per_step": 2 * M * N, "streams": 2,
-                    "call": "gemm_bf16_run_host (H2D A,B + GEMM + D2H D per step)"},
+                    "call": "gemm_bf16_run_host (H2D A,B + GEMM + D2H D per step)",
+                    "bound": "host link", "copies_only_value": copy_bound,
+                    "frac_of_copy_bound": e2e_value / copy_bound},
             "gpu_launches": args.steps,
             "clocks": clock_info,
         }
