@@ -39,7 +39,7 @@ L2_BYTES = 129e6
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="cube8192")
@@ -377,11 +377,13 @@ def run_ours(args):
             raise RuntimeError(f"device watchdog tripped in the end-to-end loop: {detail:#x}")
     gs[1].close()
 
-    # The GEMM kernel is timed alone (back-to-back launches of one kernel), so
-    # the roofline denominator is the measured burst bf16 figure.
+    # The timed region is seconds of back-to-back launches under the GPU's
+    # power cap -- the condition of the sustained cuBLAS figure (a back-to-back
+    # loop of seconds), so that is the roofline denominator; the fraction of
+    # the burst figure (best single launches) is reported beside it.
     peaks, peak_src = load_peaks()
-    peak = peaks.get("bf16_tflops")
-    peak_sustained = peaks.get("bf16_tflops_sustained")
+    peak_burst = peaks.get("bf16_tflops")
+    peak = peaks.get("bf16_tflops_sustained")
     kernel_tag = f"gemm_ws_c{info['cta_group']}"
     achieved = flops / (kernel_ms * 1e-3) / 1e12
     traffic = profiled_traffic(kernel_tag, args.workload)
@@ -400,13 +402,16 @@ def run_ours(args):
             "config": workload_config(args.workload, info),
             "pct_of_dense_bf16_peak": {
                 "nominal_2250_tflops": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
-                f"{peak_src}_burst": 100.0 * value / world / peak,
-                f"{peak_src}_sustained": 100.0 * value / world / peak_sustained,
+                f"{peak_src}_burst": 100.0 * value / world / peak_burst,
+                f"{peak_src}_sustained": 100.0 * value / world / peak,
             },
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": kernel_tag, "kernel_ms": kernel_ms,
-                         "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)"},
+                         "timed_seconds": kernel_ms * args.steps * 1e-3,
+                         "peak_source": f"{peak_src} bf16_tflops_sustained (back-to-back loop of seconds under "
+                                        f"the power cap, as the timed region here)",
+                         "frac_of_burst_peak": achieved / peak_burst},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * (M * K + N * K),
                     "d2h_bytes_per_step": 2 * M * N, "streams": 2,

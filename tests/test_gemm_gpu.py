@@ -457,6 +457,16 @@ def test_very_large_m_or_n(M, N, K):
     check(D, A, B, M, N, K, rows=rows, exact=True)
 
 
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_very_long_k(cta_group):
+    # 16,385 k-blocks in one tile, the last holding 8 valid columns: every fp32
+    # partial sum of integers in [-2, 2] stays below 2^24, so the result is exact
+    M, N, K = 130, 130, (1 << 20) + 8
+    A, B = inputs.make_problem(M, N, K, "int2", seed=67)
+    D = run_gpu(A, B, M, N, K, cta_group=cta_group)
+    check(D, A, B, M, N, K, rows=np.array([0, 1, 63, 127, 128, 129]), exact=True)
+
+
 def run_fused_gpu(A, B, M, N, K, C=None, bias=None, alpha=1.0, beta=0.0, ldd=None, inplace=False, **opts):
     ldd = N if ldd is None else ldd
     dev = torch.device("cuda:0")
