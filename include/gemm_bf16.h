@@ -124,12 +124,20 @@ typedef enum gemm_bf16_option {
                                         tensor-memory accumulator g, i.e. every other tile (a warp:
                                         32 rows x 256 columns); needs ACC_BUFFERS = 2, else plan
                                         fails with INVALID_ARG */
-    GEMM_BF16_OPT_SCHEDULER = 16      /* WS kernel's tile order.  0 (default) = static: each SM
+    GEMM_BF16_OPT_SCHEDULER = 16,     /* WS kernel's tile order.  0 (default) = static: each SM
                                         (pair) walks the grid-stride sequence.  1 = dynamic: after
                                         its stream-K share, each SM (pair) takes the next whole tile
                                         from a device counter owned by the handle, so faster SMs
                                         take more tiles; the last SM (pair) to finish resets the
                                         counter, so launches of one handle must not overlap */
+    GEMM_BF16_OPT_REPACK = 17         /* operands whose row pitch (lda or ldb, in bytes) is not a
+                                        multiple of 128: TMA then reads each 128-byte box row as two
+                                        L2 lines and the GEMM slows by ~28%.  Such an operand can be
+                                        copied first (one HBM read + write, same stream) into a
+                                        handle-owned buffer with a 128-byte-multiple pitch.
+                                        0 (default) = automatic: A when N >= 4096, B when M >= 4096
+                                        (where the GEMM's saving exceeds the copy);
+                                        1 = always when misaligned; 2 = never */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */
@@ -156,6 +164,8 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t sk_tiles;             /* tiles split along k (stream-K); 0 = none */
     int32_t epi_schedule;         /* 0 = cooperative, 1 = ping-pong */
     int32_t scheduler;            /* 0 = static, 1 = dynamic */
+    int32_t repack;               /* operands copied to an aligned pitch: bit 0 = A, bit 1 = B */
+    int32_t packed_ld;            /* their pitch in elements (K rounded up to 64); 0 = none */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's

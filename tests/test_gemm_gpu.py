@@ -242,6 +242,59 @@ def test_dynamic_scheduler_recovers_after_watchdog_timeout():
             check(dD.cpu(), A, B, M, N, K, exact=True)
 
 
+@pytest.mark.parametrize("M,N,K,lda,ldb", [
+    (1000, 900, 1000, 1008, 1000),   # both pitches misaligned (2016 B, 2000 B)
+    (300, 520, 1001, 1008, 1064),    # k tail of one element in the copy
+    (129, 257, 8, 8, 16),            # one short k-block, 16- and 32-byte pitches
+    (640, 384, 4104, 4104, 4160),    # only A misaligned
+])
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_repacked_operands_exact(M, N, K, lda, ldb, cta_group):
+    A, B = inputs.make_problem(M, N, K, "int2", seed=K + lda, lda=lda, ldb=ldb)
+    with binding.Gemm(0, repack=1, cta_group=cta_group) as g:
+        info = g.plan(M, N, K, lda, ldb, N)
+    want = (1 if (lda * 2) % 128 else 0) | (2 if (ldb * 2) % 128 else 0)
+    assert info["repack"] == want and info["packed_ld"] == (K + 63) // 64 * 64
+    D = run_gpu(A, B, M, N, K, repack=1, cta_group=cta_group)
+    check(D, A, B, M, N, K, exact=True)
+    D0 = run_gpu(A, B, M, N, K, repack=2, cta_group=cta_group)
+    assert torch.equal(D.view(torch.int16), D0.view(torch.int16))
+
+
+def test_repack_copies_every_run_and_auto_rule():
+    # automatic mode: A is copied when N >= 4096, B when M >= 4096
+    M, N, K = 4100, 4200, 520
+    A, B = inputs.make_problem(M, N, K, "int2", seed=91)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    rows = sample_rows(M, extra=8)
+    with binding.Gemm(0) as g:
+        assert g.plan(M, N, K)["repack"] == 3  # 1040-byte pitches
+        g.run(dA, dB, dD)
+        torch.cuda.synchronize()
+        check(dD.cpu(), A, B, M, N, K, rows=rows, exact=True)
+        # new operand values: the copy must be taken again
+        A2 = (A.float() * -1).to(torch.bfloat16)
+        dA.copy_(A2)
+        g.run(dA, dB, dD)
+        g.run_fused(dA, dB, dD, dD, None, 1.0, 1.0)  # D = A2 B^T + (A2 B^T) = 2 A2 B^T
+        assert g.device_status()[0] == binding.OK
+    torch.cuda.synchronize()
+    check((dD.cpu().float() / 2).to(torch.bfloat16), A2, B, M, N, K, rows=rows, exact=True)
+    with binding.Gemm(0) as g:
+        assert g.plan(M, 1000, K)["repack"] == 2   # N < 4096: A stays, B (M >= 4096) is copied
+        assert g.plan(1000, N, K)["repack"] == 1
+        assert g.plan(M, N, 512)["repack"] == 0    # 1024-byte pitches are aligned
+
+
+def test_ragged_workload_is_repacked_automatically():
+    w = inputs.WORKLOADS["ragged"]
+    with binding.Gemm(0) as g:
+        info = g.plan(w["M"], w["N"], w["K"])
+    assert info["repack"] == 3 and info["packed_ld"] == 4160
+
+
 def test_stream_k_random_inputs_and_repeated_launches():
     # flags carry a per-launch epoch: back-to-back launches on one handle must
     # not read a previous launch's partials

@@ -15,7 +15,9 @@ stage ring with __syncthreads up to the default kernel:
   +streamk    the partial last wave of tiles split along k (the default)
 
 With --schedules the default kernel is compared with its schedule options
-instead: the ping-pong epilogue, the dynamic tile counter, and both.
+instead: the ping-pong epilogue, the dynamic tile counter, and both.  With
+--variant NAME:OPT=V,OPT=V (repeatable) any named option sets are compared,
+e.g. --variant aligned:repack=0 --variant unaligned:repack=2.
 
 Rungs run interleaved in shuffled order for several rounds (the GPU's power
 limit moves the clock between runs) and the best and median times are printed
@@ -61,7 +63,18 @@ def main(argv=None) -> int:
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--device", type=int, default=0)
     ap.add_argument("--schedules", action="store_true", help="compare the schedule options")
+    ap.add_argument("--variant", action="append", default=[], metavar="NAME:OPT=V,...",
+                    help="compare named option sets instead of the ladder")
     args = ap.parse_args(argv)
+    rungs = RUNGS
+    if args.schedules:
+        rungs = SCHEDULE_RUNGS
+    if args.variant:
+        rungs = []
+        for spec in args.variant:
+            name, _, opts = spec.partition(":")
+            kv = dict(item.split("=", 1) for item in opts.split(",") if item)
+            rungs.append((name, {k: int(v) for k, v in kv.items()}))
 
     libbuild.build()
     torch.cuda.set_device(args.device)
@@ -72,7 +85,7 @@ def main(argv=None) -> int:
     dA, dB = A.to(dev), B.to(dev)
     dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     handles = []
-    for name, opts in (SCHEDULE_RUNGS if args.schedules else RUNGS):
+    for name, opts in rungs:
         g = binding.Gemm(args.device, **opts)
         handles.append((name, g, g.plan(M, N, K)))
 
@@ -106,7 +119,8 @@ def main(argv=None) -> int:
         print(json.dumps({"workload": args.workload, "rung": name, "best_ms": round(best, 4),
                           "median_ms": round(med, 4), "tflops_best": round(flops / best / 1e9, 1),
                           "tflops_median": round(flops / med / 1e9, 1), "grid": info["grid_ctas"],
-                          "stages": info["stages"], "sk_tiles": info["sk_tiles"], "status": st}))
+                          "stages": info["stages"], "sk_tiles": info["sk_tiles"], "repack": info["repack"],
+                          "status": st}))
         g.close()
     return rc
 

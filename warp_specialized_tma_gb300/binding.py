@@ -48,6 +48,7 @@ OPTIONS = {
     "pdl": 14,
     "epi_schedule": 15,
     "scheduler": 16,
+    "repack": 17,
 }
 
 # the C entry points and their signatures
@@ -97,6 +98,8 @@ class PlanInfo(ctypes.Structure):
         ("sk_tiles", ctypes.c_int32),
         ("epi_schedule", ctypes.c_int32),
         ("scheduler", ctypes.c_int32),
+        ("repack", ctypes.c_int32),
+        ("packed_ld", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -20,7 +20,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 17;
+constexpr int kNumOptions = 18;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 
 struct Plan {
@@ -38,6 +38,8 @@ struct Plan {
     int epilogue_opt = 0;
     int epi_pingpong = 0;
     int sched_dynamic = 0;
+    bool repack_a = false, repack_b = false;  // operands copied to a 128-byte-multiple pitch first
+    int64_t ldp = 0;                          // that pitch in elements
     int64_t tiles = 0;
     int num_m_blocks = 0, num_n_blocks = 0, num_k_blocks = 0;
     int grid_ctas = 0;
@@ -73,6 +75,9 @@ struct gemm_bf16 {
     uint32_t *ws_flags = nullptr;
     size_t ws_slots = 0;
     uint32_t epoch = 0;
+    // packed operand copies (A then B), grown on demand by plan
+    void *pack = nullptr;
+    size_t pack_bytes = 0;
 };
 
 namespace {
@@ -96,6 +101,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_PDL: return 1;
     case GEMM_BF16_OPT_EPI_SCHEDULE: return 0;
     case GEMM_BF16_OPT_SCHEDULER: return 0;
+    case GEMM_BF16_OPT_REPACK: return 0;
     default: return 0;
     }
 }
@@ -119,6 +125,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_PDL: return v == 0 || v == 1;
     case GEMM_BF16_OPT_EPI_SCHEDULE: return v == 0 || v == 1;
     case GEMM_BF16_OPT_SCHEDULER: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_REPACK: return v >= 0 && v <= 2;
     default: return false;
     }
 }
@@ -274,6 +281,8 @@ GEMM_BF16_API int gemm_bf16_destroy(gemm_bf16_t h)
         cudaFree(h->ws);
     if (h->ws_flags)
         cudaFree(h->ws_flags);
+    if (h->pack)
+        cudaFree(h->pack);
     delete h;
     return GEMM_BF16_OK;
 }
@@ -459,6 +468,36 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         h->ws_flags = nflags;
         h->ws_slots = (size_t)pl.grid_ctas;
     }
+    // Operand repacking: a row pitch that is not a multiple of 128 bytes makes
+    // every TMA box row straddle two L2 lines (~28% slower GEMM, measured).  A
+    // copy costs one HBM read + write of the operand, i.e. time ~ rows * K,
+    // while the GEMM's saving grows with rows * K * (other dimension): it pays
+    // once the other dimension is >= 4096 (automatic mode).
+    {
+        const int64_t mode = h->opt[GEMM_BF16_OPT_REPACK];
+        const bool mis_a = (lda * 2) % 128 != 0, mis_b = (ldb * 2) % 128 != 0;
+        pl.repack_a = mis_a && (mode == 1 || (mode == 0 && N >= 4096));
+        pl.repack_b = mis_b && (mode == 1 || (mode == 0 && M >= 4096));
+        if (pl.repack_a || pl.repack_b) {
+            pl.ldp = (K + 63) / 64 * 64;
+            const size_t need = (size_t)((pl.repack_a ? M : 0) + (pl.repack_b ? N : 0)) * (size_t)pl.ldp * 2;
+            if (need > h->pack_bytes) {
+                void *np = nullptr;
+                if (cudaMalloc(&np, need) != cudaSuccess) {
+                    cudaGetLastError();
+                    if (mode == 1)
+                        return GEMM_BF16_ERR_CUDA;
+                    pl.repack_a = pl.repack_b = false;  // automatic: run on the original pitch
+                    pl.ldp = 0;
+                } else {
+                    if (h->pack)
+                        cudaFree(h->pack);
+                    h->pack = np;
+                    h->pack_bytes = need;
+                }
+            }
+        }
+    }
     pl.valid = true;
     h->plan = pl;
     return GEMM_BF16_OK;
@@ -494,6 +533,8 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->regs_per_thread = p.regs;
     info->epi_schedule = p.epi_pingpong;
     info->scheduler = p.sched_dynamic;
+    info->repack = (p.repack_a ? 1 : 0) | (p.repack_b ? 2 : 0);
+    info->packed_ld = (int32_t)p.ldp;
     return GEMM_BF16_OK;
 }
 
@@ -533,10 +574,20 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     if (rc != GEMM_BF16_OK)
         return rc;
 
-    if (!h->maps_valid || h->mA != A || h->mB != B || h->mD != D) {
+    // Operands routed through the packed buffer are copied first, on the same
+    // stream; the GEMM's tensor maps then describe the packed copies.
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *pack_a = pl.repack_a ? h->pack : nullptr;
+    void *pack_b = pl.repack_b ? static_cast<uint16_t *>(h->pack) + (pl.repack_a ? pl.M * pl.ldp : 0) : nullptr;
+    const void *Ae = pack_a ? pack_a : A;
+    const void *Be = pack_b ? pack_b : B;
+    const int64_t lda_e = pack_a ? pl.ldp : pl.lda;
+    const int64_t ldb_e = pack_b ? pl.ldp : pl.ldb;
+
+    if (!h->maps_valid || h->mA != Ae || h->mB != Be || h->mD != D) {
         const uint32_t b_rows = (uint32_t)(kBlockN / pl.cta_group);
-        if ((rc = encode_2d(&h->tmA, A, (uint64_t)pl.K, (uint64_t)pl.M, (uint64_t)pl.lda * 2, kBlockK, kBlockM)) ||
-            (rc = encode_2d(&h->tmB, B, (uint64_t)pl.K, (uint64_t)pl.N, (uint64_t)pl.ldb * 2, kBlockK, b_rows))) {
+        if ((rc = encode_2d(&h->tmA, Ae, (uint64_t)pl.K, (uint64_t)pl.M, (uint64_t)lda_e * 2, kBlockK, kBlockM)) ||
+            (rc = encode_2d(&h->tmB, Be, (uint64_t)pl.K, (uint64_t)pl.N, (uint64_t)ldb_e * 2, kBlockK, b_rows))) {
             h->maps_valid = false;
             return rc;
         }
@@ -548,8 +599,18 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
         } else {
             std::memset(&h->tmD, 0, sizeof(h->tmD));  // never dereferenced on the masked path
         }
-        h->mA = A, h->mB = B, h->mD = D;
+        h->mA = Ae, h->mB = Be, h->mD = D;
         h->maps_valid = true;
+    }
+    if (pack_a || pack_b) {
+        RepackJob jobs[2];
+        int nj = 0;
+        if (pack_a)
+            jobs[nj++] = {A, pack_a, pl.lda, pl.ldp, pl.M, pl.K};
+        if (pack_b)
+            jobs[nj++] = {B, pack_b, pl.ldb, pl.ldp, pl.N, pl.K};
+        if (launch_repack(jobs, nj, h->num_sms, st) != 0)
+            return GEMM_BF16_ERR_CUDA;
     }
 
     GemmParams prm;
@@ -611,7 +672,7 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     cfg.gridDim = dim3((unsigned)pl.grid_ctas, 1, 1);
     cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = static_cast<cudaStream_t>(stream);
+    cfg.stream = st;
     if (pl.cta_group == 2) {
         attr[nattr].id = cudaLaunchAttributeClusterDimension;
         attr[nattr].val.clusterDim.x = 2;

@@ -91,4 +91,14 @@ const void *ws_kernel_c1(bool setmaxnreg);
 const void *ws_kernel_c2(bool setmaxnreg);
 const void *nows_kernel(bool mbar_war);
 
+// One operand copy: `rows` rows of `cols` bf16 from pitch ld_src to pitch
+// ld_dst (elements; both multiples of 8, both bases 16-byte aligned).
+struct RepackJob {
+    const void *src;
+    void *dst;
+    int64_t ld_src, ld_dst, rows, cols;
+};
+// Runs one or two copies in one launch on `stream`; returns a cudaError_t value.
+int launch_repack(const RepackJob *jobs, int njobs, int num_sms, cudaStream_t stream);
+
 }  // namespace wstma
