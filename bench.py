@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="cube8192")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-comparator", dest="comparator", action="store_false",
+                    help="skip timing torch.matmul (cuBLAS) as a library comparator")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target duration of the CPU-oracle baseline sample")
     return ap.parse_args()
@@ -318,7 +320,8 @@ def run_ours(args):
         raise RuntimeError(f"device watchdog tripped in the timed region: {detail:#x}")
     ms_total = t_begin.elapsed_time(t_end)
     max_ms = dist.max(ms_total, dev)
-    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = statistics.fmean(launch_ms)
     value = aggregate(flops, args.steps, max_ms, world)
 
     # End to end through the C ABI with host operands (pinned): every step copies
@@ -351,8 +354,57 @@ def run_ours(args):
     e2e_ms = dist.max(e0.elapsed_time(e1), dev)
     e2e_value = aggregate(flops, args.e2e_steps, e2e_ms, world)
 
+    # Library comparator (not an oracle): cuBLAS through torch.matmul on the
+    # same device operands, outside the timed region above.  The GPU's clock
+    # under its power cap depends on what ran just before, so the comparator and
+    # this kernel run in alternating back-to-back loops (ours, cuBLAS, cuBLAS,
+    # ours, ...) of the same total length, and both rates are reported.
+    lib_tflops = ours_alt = None
+    if args.comparator:
+        dD2 = torch.empty_like(dD)
+        for _ in range(max(args.warmup, 3)):
+            torch.matmul(dA, dB.t(), out=dD2)
+        torch.cuda.synchronize(dev)
+        chunk = max(1, args.steps // 4)
+        t_lib = t_ours = 0.0
+
+        def loop(fn):
+            l0 = torch.cuda.Event(enable_timing=True)
+            l1 = torch.cuda.Event(enable_timing=True)
+            l0.record(stream)
+            for _ in range(chunk):
+                fn()
+            l1.record(stream)
+            torch.cuda.synchronize(dev)
+            return l0.elapsed_time(l1)
+
+        ours_fn = lambda: g.run(dA, dB, dD, stream)  # noqa: E731
+        lib_fn = lambda: torch.matmul(dA, dB.t(), out=dD2)  # noqa: E731
+        for c in range(4):
+            for fn in ((ours_fn, lib_fn) if c % 2 == 0 else (lib_fn, ours_fn)):
+                ms = loop(fn)
+                if fn is lib_fn:
+                    t_lib += ms
+                else:
+                    t_ours += ms
+        lib_tflops = flops * 4 * chunk / (t_lib * 1e-3) / 1e12
+        ours_alt = flops * 4 * chunk / (t_ours * 1e-3) / 1e12
+        st2, detail2 = g.device_status()
+        if st2 != binding.OK:
+            raise RuntimeError(f"device watchdog tripped in the comparator loops: {detail2:#x}")
+        del dD2
+
     # The same host <-> device copies with no GEMM, scheduled the same way: the
     # host link's bound on the end-to-end rate (a link measurement, no kernel).
+    def copies(i):
+        j = i % 2
+        with torch.cuda.stream(streams[j]):
+            bufs[j][0].copy_(hA, non_blocking=True)
+            bufs[j][1].copy_(hB, non_blocking=True)
+            hDs[j].copy_(bufs[j][2], non_blocking=True)
+
+    for i in range(4):
+        copies(i)
     torch.cuda.synchronize(dev)
     c0 = torch.cuda.Event(enable_timing=True)
     c1 = torch.cuda.Event(enable_timing=True)
@@ -361,11 +413,7 @@ def run_ours(args):
     c0.record(streams[0])
     streams[1].wait_event(c0)
     for i in range(args.e2e_steps):
-        j = i % 2
-        with torch.cuda.stream(streams[j]):
-            bufs[j][0].copy_(hA, non_blocking=True)
-            bufs[j][1].copy_(hB, non_blocking=True)
-            hDs[j].copy_(bufs[j][2], non_blocking=True)
+        copies(i)
     streams[0].wait_stream(streams[1])
     c1.record(streams[0])
     torch.cuda.synchronize(dev)
@@ -418,6 +466,16 @@ def run_ours(args):
                     "call": "gemm_bf16_run_host (H2D A,B + GEMM + D2H D per step)",
                     "bound": "host link", "copies_only_value": copy_bound,
                     "frac_of_copy_bound": e2e_value / copy_bound},
+            "detail": {
+                "launch_ms": {"mean": kernel_ms, "median": statistics.median(launch_ms), "best": min(launch_ms)},
+                "tflops_best_launch": flops / (min(launch_ms) * 1e-3) / 1e12,
+                "hbm_gbs_compulsory": 2.0 * (M * K + N * K + M * N) / (kernel_ms * 1e-3) / 1e9,
+                "library_comparator": None if lib_tflops is None else {
+                    "what": "torch.matmul(A, B.T) (cuBLAS), same operands; alternating back-to-back loops "
+                            "with this kernel, each side " + str(4 * max(1, args.steps // 4)) + " launches",
+                    "value": lib_tflops, "ours_in_the_same_loops": ours_alt,
+                    "ratio_ours_to_library": ours_alt / lib_tflops, "unit": UNIT},
+            },
             "gpu_launches": args.steps,
             "clocks": clock_info,
         }
