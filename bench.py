@@ -164,7 +164,7 @@ class ClockSampler:
 
 def profiled_traffic(kernel_tag: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current kernel (its device code and planner, build.kernel_digest), else None."""
     from warp_specialized_tma_gb300 import build as libbuild
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.traffic.txt")
     try:
@@ -174,7 +174,7 @@ def profiled_traffic(kernel_tag: str, workload: str):
                 if "=" in line and not line.startswith("#"):
                     k, v = line.split("=", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("source_digest") != libbuild.source_digest():
+        if kv.get("kernel_digest") != libbuild.kernel_digest():
             return None
         return int(float(kv["dram_bytes_per_launch"]))
     except (OSError, KeyError, ValueError):

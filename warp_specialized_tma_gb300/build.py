@@ -47,6 +47,23 @@ def source_digest() -> str:
     return h.hexdigest()
 
 
+# What decides the GEMM kernel's behaviour on a given problem: its device code
+# and the host planner that picks its launch shape (not the public header's
+# documentation, the binding or the other kernels).
+KERNEL_FILES = ["gemm_ws.cuh", "gemm_common.cuh", "ptx.cuh", "gemm_kernels.h", "gemm_ws_c1.cu", "gemm_ws_c2.cu",
+                "gemm_bf16_api.cu"]
+
+
+def kernel_digest() -> str:
+    """sha256 over the files in KERNEL_FILES: identifies a measured kernel."""
+    h = hashlib.sha256()
+    for name in KERNEL_FILES:
+        with open(os.path.join(CSRC, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def _stamp_path() -> str:
     return os.path.join(BUILD_DIR, "stamp.txt")
 
