@@ -130,7 +130,7 @@ typedef enum gemm_bf16_option {
                                         from a device counter owned by the handle, so faster SMs
                                         take more tiles; the last SM (pair) to finish resets the
                                         counter, so launches of one handle must not overlap */
-    GEMM_BF16_OPT_REPACK = 17         /* operands whose row pitch (lda or ldb, in bytes) is not a
+    GEMM_BF16_OPT_REPACK = 17,        /* operands whose row pitch (lda or ldb, in bytes) is not a
                                         multiple of 128: TMA then reads each 128-byte box row as two
                                         L2 lines and the GEMM slows by ~28%.  Such an operand can be
                                         copied first (one HBM read + write, same stream) into a
@@ -138,6 +138,13 @@ typedef enum gemm_bf16_option {
                                         0 (default) = automatic: A when N >= 4096, B when M >= 4096
                                         (where the GEMM's saving exceeds the copy);
                                         1 = always when misaligned; 2 = never */
+    GEMM_BF16_OPT_K_ORDER = 18        /* WS kernel's k direction per whole tile.  0 = ascending;
+                                        1 (default) = alternating: each SM (pair)'s odd-numbered whole tiles load
+                                        their k-blocks last to first, so a wave starts on the operand
+                                        slices the previous wave loaded last (still in L2).  Changes
+                                        only the fp32 summation order (within the rounding bound;
+                                        results stay deterministic).  Measured on 8192^3: DRAM reads
+                                        -15%, and under the power cap +1% throughput */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */
@@ -166,6 +173,7 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t scheduler;            /* 0 = static, 1 = dynamic */
     int32_t repack;               /* operands copied to an aligned pitch: bit 0 = A, bit 1 = B */
     int32_t packed_ld;            /* their pitch in elements (K rounded up to 64); 0 = none */
+    int32_t k_order;              /* 0 = ascending, 1 = alternating */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's

@@ -124,6 +124,8 @@ MID = [(256, 256, 256), (300, 520, 200), (129, 257, 65), (640, 384, 1000), (1000
     dict(cta_group=2, scheduler=1),
     dict(cta_group=2, epi_schedule=1, scheduler=1),
     dict(cta_group=2, scheduler=1, persistent=0),
+    dict(cta_group=1, k_order=0),
+    dict(cta_group=2, k_order=0),
     dict(pipeline=binding.PIPE_SYNC_WAR),
     dict(pipeline=binding.PIPE_MBAR_WAR),
 ])
@@ -165,7 +167,8 @@ def test_stream_k_split_tiles_exact(cta_group, M, N, K, max_ctas):
     assert torch.equal(D.view(torch.int16), D0.view(torch.int16))
 
 
-SCHEDULES = [dict(epi_schedule=1), dict(scheduler=1), dict(epi_schedule=1, scheduler=1)]
+SCHEDULES = [dict(epi_schedule=1), dict(scheduler=1), dict(epi_schedule=1, scheduler=1), dict(k_order=0),
+             dict(k_order=0, scheduler=1)]
 
 
 @pytest.mark.parametrize("cta_group", [1, 2])
@@ -185,6 +188,7 @@ def test_schedules_few_ctas_many_tiles_repeated(cta_group, sched, max_ctas, K):
         info = g.plan(M, N, K)
         assert info["epi_schedule"] == sched.get("epi_schedule", 0)
         assert info["scheduler"] == sched.get("scheduler", 0)
+        assert info["k_order"] == sched.get("k_order", 1)
         for _ in range(4):
             D = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=dev)
             g.run(dA, dB, D)

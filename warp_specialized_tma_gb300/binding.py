@@ -49,6 +49,7 @@ OPTIONS = {
     "epi_schedule": 15,
     "scheduler": 16,
     "repack": 17,
+    "k_order": 18,
 }
 
 # the C entry points and their signatures
@@ -100,6 +101,7 @@ class PlanInfo(ctypes.Structure):
         ("scheduler", ctypes.c_int32),
         ("repack", ctypes.c_int32),
         ("packed_ld", ctypes.c_int32),
+        ("k_order", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

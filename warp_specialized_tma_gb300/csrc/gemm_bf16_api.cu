@@ -20,7 +20,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 18;
+constexpr int kNumOptions = 19;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 
 struct Plan {
@@ -38,6 +38,7 @@ struct Plan {
     int epilogue_opt = 0;
     int epi_pingpong = 0;
     int sched_dynamic = 0;
+    int k_order = 0;
     bool repack_a = false, repack_b = false;  // operands copied to a 128-byte-multiple pitch first
     int64_t ldp = 0;                          // that pitch in elements
     int64_t tiles = 0;
@@ -102,6 +103,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_EPI_SCHEDULE: return 0;
     case GEMM_BF16_OPT_SCHEDULER: return 0;
     case GEMM_BF16_OPT_REPACK: return 0;
+    case GEMM_BF16_OPT_K_ORDER: return 1;
     default: return 0;
     }
 }
@@ -126,6 +128,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_EPI_SCHEDULE: return v == 0 || v == 1;
     case GEMM_BF16_OPT_SCHEDULER: return v == 0 || v == 1;
     case GEMM_BF16_OPT_REPACK: return v >= 0 && v <= 2;
+    case GEMM_BF16_OPT_K_ORDER: return v == 0 || v == 1;
     default: return false;
     }
 }
@@ -326,6 +329,7 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
     pl.epilogue_opt = (int)h->opt[GEMM_BF16_OPT_EPILOGUE];
     pl.epi_pingpong = (int)h->opt[GEMM_BF16_OPT_EPI_SCHEDULE];
     pl.sched_dynamic = (int)h->opt[GEMM_BF16_OPT_SCHEDULER];
+    pl.k_order = (int)h->opt[GEMM_BF16_OPT_K_ORDER];
     pl.fault_skip = (int)h->opt[GEMM_BF16_OPT_FAULT_SKIP_LOAD];
     pl.watchdog_ns = (uint64_t)h->opt[GEMM_BF16_OPT_WATCHDOG_NS];
     pl.epi_tma_allowed = ((ldd * 2) % 16) == 0;
@@ -341,6 +345,7 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         pl.setmaxnreg = 0;
         pl.epi_pingpong = 0;
         pl.sched_dynamic = 0;
+        pl.k_order = 0;
     } else if (cg == 0) {
         cg = 2;  // an SM pair per 256x256 tile halves each SM's operand traffic
     }
@@ -535,6 +540,7 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->scheduler = p.sched_dynamic;
     info->repack = (p.repack_a ? 1 : 0) | (p.repack_b ? 2 : 0);
     info->packed_ld = (int32_t)p.ldp;
+    info->k_order = p.k_order;
     return GEMM_BF16_OK;
 }
 
@@ -647,6 +653,7 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     prm.epi_pingpong = pl.epi_pingpong;
     prm.sched_dynamic = pl.sched_dynamic;
     prm.sched = h->d_err + 2;
+    prm.k_order = pl.k_order;
     if (fz) {
         prm.fused = kFusedOn;
         prm.alpha = fz->alpha;

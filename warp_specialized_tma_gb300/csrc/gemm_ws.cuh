@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             uint32_t ph = 0;
             int32_t it = 0;
             int32_t seq = 0;
+            int32_t whole = 0;  // whole-tile items so far: their parity picks the k direction
             bool ok = true;
             bool counter_done = false;
             WorkIter wi;
@@ -201,6 +202,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 const TileCoord tc = tile_coord(w.tile, p);
                 const int32_t ya = tc.mb * kTileM + (int32_t)rank * kBlockM;
                 const int32_t yb = tc.nb * kBlockN + (int32_t)rank * (int32_t)kBRows;
+                // Alternating k direction: all SM pairs are in the same wave of whole
+                // tiles at about the same time, and consecutive waves of a band share
+                // their A panels.  A wave that walks k in the opposite direction to
+                // the previous one starts on the k-slices that wave loaded last, which
+                // are still in L2.  The MMA side only counts k-blocks (accumulation
+                // starts at the first one it is given), so only the loads change.
+                const bool whole_tile = w.kb0 == 0 && w.kb1 == KB;
+                const bool rev = p.k_order == 1 && whole_tile && (whole & 1);
+                whole += whole_tile ? 1 : 0;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     // wait until the MMAs that read this stage (group) one lap ago
                     // have retired; a group of G stages is released by one commit
@@ -212,7 +222,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     }
                     const uint32_t fb = full_target + 8u * s;
                     const uint32_t sa = stage0 + (uint32_t)s * kStageBytes;
-                    const int32_t x = kb * kBlockK;
+                    const int32_t x = (rev ? w.kb0 + w.kb1 - 1 - kb : kb) * kBlockK;
                     if (it != p.fault_skip_it) {
                         if (!kCluster || rank == 0)
                             mbar_arrive_expect_tx(full_bar + 8u * s, kTxBytes);
