@@ -404,14 +404,15 @@ def run_ours(args):
             raise RuntimeError(f"device watchdog tripped in the comparator loops: {detail2:#x}")
         del dD2
 
-    # The same host <-> device copies with no GEMM, scheduled the same way: the
-    # host link's bound on the end-to-end rate (a link measurement, no kernel).
+    # The host link's bound on the end-to-end rate (a link measurement, no
+    # kernel): a step's bytes moved on the link's best schedule -- A and B
+    # host -> device on one stream while a D goes device -> host on the other.
     def copies(i):
-        j = i % 2
-        with torch.cuda.stream(streams[j]):
-            bufs[j][0].copy_(hA, non_blocking=True)
-            bufs[j][1].copy_(hB, non_blocking=True)
-            hDs[j].copy_(bufs[j][2], non_blocking=True)
+        with torch.cuda.stream(streams[0]):
+            bufs[0][0].copy_(hA, non_blocking=True)
+            bufs[0][1].copy_(hB, non_blocking=True)
+        with torch.cuda.stream(streams[1]):
+            hDs[1].copy_(bufs[1][2], non_blocking=True)
 
     for i in range(4):
         copies(i)

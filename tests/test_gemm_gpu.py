@@ -331,11 +331,24 @@ def test_epilogue_paths_and_padding(N, epilogue, ldd):
     check(D, A, B, M, N, K)
 
 
+@pytest.mark.parametrize("serpentine", [0, 1])
 @pytest.mark.parametrize("raster_group", [0, 1, 3, 8, 64])
-def test_raster_orders(raster_group):
+def test_raster_orders(raster_group, serpentine):
     M, N, K = 1536, 1280, 128
     A, B = inputs.make_problem(M, N, K, "int2", seed=3)
-    check(run_gpu(A, B, M, N, K, raster_group=raster_group, max_ctas=10), A, B, M, N, K, exact=True)
+    D = run_gpu(A, B, M, N, K, raster_group=raster_group, serpentine=serpentine, max_ctas=10)
+    check(D, A, B, M, N, K, exact=True)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_serpentine_with_stream_k_and_pipelines(cta_group):
+    # odd bands reversed, split tiles, ragged edges; and the ablation loops
+    M, N, K = 2000, 1800, 700
+    A, B = inputs.make_problem(M, N, K, "int2", seed=13, lda=pad8(K), ldb=pad8(K))
+    check(run_gpu(A, B, M, N, K, serpentine=1, raster_group=2, max_ctas=14, cta_group=cta_group),
+          A, B, M, N, K, exact=True)
+    check(run_gpu(A, B, M, N, K, serpentine=1, raster_group=2, pipeline=binding.PIPE_MBAR_WAR),
+          A, B, M, N, K, exact=True)
 
 
 def test_identity_and_permutation_full_tiles():

@@ -13,7 +13,8 @@ stage ring with __syncthreads up to the default kernel:
   +setmaxnreg producer warps give registers to the epilogue warps
   +2cta       an SM pair per 256x256 tile (cta_group::2)
   +streamk    the partial last wave of tiles split along k
-  +k-alt      consecutive whole tiles walk k in alternating directions (the default)
+  +k-alt      consecutive whole tiles walk k in alternating directions
+  +serpentine odd tile bands walk their columns right to left (the default)
 
 With --schedules the default kernel is compared with its schedule options
 instead: the ping-pong epilogue, the dynamic tile counter, and both.  With
@@ -38,15 +39,16 @@ from . import binding, inputs
 from . import build as libbuild
 
 RUNGS = [
-    ("sync_war", dict(pipeline=binding.PIPE_SYNC_WAR)),
-    ("mbar_war", dict(pipeline=binding.PIPE_MBAR_WAR)),
-    ("ws", dict(cta_group=1, persistent=0, acc_buffers=1, stream_k=0, k_order=0)),
-    ("+persistent", dict(cta_group=1, persistent=1, acc_buffers=1, stream_k=0, k_order=0)),
-    ("+tmem2", dict(cta_group=1, acc_buffers=2, stream_k=0, k_order=0)),
-    ("+setmaxnreg", dict(cta_group=1, acc_buffers=2, setmaxnreg=1, stream_k=0, k_order=0)),
-    ("+2cta", dict(cta_group=2, setmaxnreg=0, stream_k=0, k_order=0)),
-    ("+streamk", dict(k_order=0)),
-    ("+k-alt", dict()),
+    ("sync_war", dict(pipeline=binding.PIPE_SYNC_WAR, serpentine=0)),
+    ("mbar_war", dict(pipeline=binding.PIPE_MBAR_WAR, serpentine=0)),
+    ("ws", dict(cta_group=1, persistent=0, acc_buffers=1, stream_k=0, k_order=0, serpentine=0)),
+    ("+persistent", dict(cta_group=1, persistent=1, acc_buffers=1, stream_k=0, k_order=0, serpentine=0)),
+    ("+tmem2", dict(cta_group=1, acc_buffers=2, stream_k=0, k_order=0, serpentine=0)),
+    ("+setmaxnreg", dict(cta_group=1, acc_buffers=2, setmaxnreg=1, stream_k=0, k_order=0, serpentine=0)),
+    ("+2cta", dict(cta_group=2, setmaxnreg=0, stream_k=0, k_order=0, serpentine=0)),
+    ("+streamk", dict(k_order=0, serpentine=0)),
+    ("+k-alt", dict(serpentine=0)),
+    ("+serpentine", dict()),
 ]
 
 

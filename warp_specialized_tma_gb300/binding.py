@@ -50,6 +50,7 @@ OPTIONS = {
     "scheduler": 16,
     "repack": 17,
     "k_order": 18,
+    "serpentine": 19,
 }
 
 # the C entry points and their signatures
@@ -102,6 +103,7 @@ class PlanInfo(ctypes.Structure):
         ("repack", ctypes.c_int32),
         ("packed_ld", ctypes.c_int32),
         ("k_order", ctypes.c_int32),
+        ("serpentine", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -20,7 +20,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 19;
+constexpr int kNumOptions = 20;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 
 struct Plan {
@@ -39,6 +39,7 @@ struct Plan {
     int epi_pingpong = 0;
     int sched_dynamic = 0;
     int k_order = 0;
+    int serpentine = 0;
     bool repack_a = false, repack_b = false;  // operands copied to a 128-byte-multiple pitch first
     int64_t ldp = 0;                          // that pitch in elements
     int64_t tiles = 0;
@@ -104,6 +105,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_SCHEDULER: return 0;
     case GEMM_BF16_OPT_REPACK: return 0;
     case GEMM_BF16_OPT_K_ORDER: return 1;
+    case GEMM_BF16_OPT_SERPENTINE: return 1;
     default: return 0;
     }
 }
@@ -129,6 +131,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_SCHEDULER: return v == 0 || v == 1;
     case GEMM_BF16_OPT_REPACK: return v >= 0 && v <= 2;
     case GEMM_BF16_OPT_K_ORDER: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_SERPENTINE: return v == 0 || v == 1;
     default: return false;
     }
 }
@@ -330,6 +333,7 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
     pl.epi_pingpong = (int)h->opt[GEMM_BF16_OPT_EPI_SCHEDULE];
     pl.sched_dynamic = (int)h->opt[GEMM_BF16_OPT_SCHEDULER];
     pl.k_order = (int)h->opt[GEMM_BF16_OPT_K_ORDER];
+    pl.serpentine = (int)h->opt[GEMM_BF16_OPT_SERPENTINE];
     pl.fault_skip = (int)h->opt[GEMM_BF16_OPT_FAULT_SKIP_LOAD];
     pl.watchdog_ns = (uint64_t)h->opt[GEMM_BF16_OPT_WATCHDOG_NS];
     pl.epi_tma_allowed = ((ldd * 2) % 16) == 0;
@@ -541,6 +545,7 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->repack = (p.repack_a ? 1 : 0) | (p.repack_b ? 2 : 0);
     info->packed_ld = (int32_t)p.ldp;
     info->k_order = p.k_order;
+    info->serpentine = p.serpentine;
     return GEMM_BF16_OK;
 }
 
@@ -654,6 +659,7 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     prm.sched_dynamic = pl.sched_dynamic;
     prm.sched = h->d_err + 2;
     prm.k_order = pl.k_order;
+    prm.serpentine = pl.serpentine;
     if (fz) {
         prm.fused = kFusedOn;
         prm.alpha = fz->alpha;

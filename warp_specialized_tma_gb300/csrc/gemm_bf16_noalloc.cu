@@ -220,6 +220,7 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     prm.sched_dynamic = 0;  // the counter lives in a handle
     prm.sched = nullptr;
     prm.k_order = 1;  // alternating k direction per whole tile, as in the default plan
+    prm.serpentine = 1;  // as in the default plan
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the status word must start at zero for this call (the array keeps the

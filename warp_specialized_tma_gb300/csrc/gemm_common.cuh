@@ -15,7 +15,9 @@ struct TileCoord {
 // Linear output-tile index -> tile coordinates.  With raster_group G > 0 the
 // tiles are walked in bands of G tile rows, column by column inside a band, so
 // the tiles that run at the same time share A and B rows in L2; G = 0 is plain
-// row-major order.
+// row-major order.  With p.serpentine, odd bands walk their columns right to
+// left: the first wave of a band then needs the B panels the last wave of the
+// previous band has just read.
 __device__ __forceinline__ TileCoord tile_coord(int32_t t, const GemmParams &p)
 {
     if (p.raster_group <= 0)
@@ -25,7 +27,8 @@ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const GemmParams &p)
     const int32_t first = band * p.raster_group;
     const int32_t rows = min(p.num_m_blocks - first, p.raster_group);
     const int32_t r = t - band * span;
-    return {first + r % rows, r / rows};
+    const int32_t col = r / rows;
+    return {first + r % rows, (p.serpentine && (band & 1)) ? p.num_n_blocks - 1 - col : col};
 }
 
 // ----------------------------------------------------------------- work items

@@ -60,6 +60,7 @@ struct GemmParams {
     int32_t sched_dynamic;  // 1 = whole tiles are taken from the counter sched[0]
     uint32_t *sched;        // [0] next whole tile, [1] clusters finished; both 0 between launches
     int32_t k_order;        // 1 = a CTA's odd-numbered whole tiles load their k-blocks last to first
+    int32_t serpentine;     // 1 = odd tile bands walk their columns right to left
 };
 
 enum : uint32_t {
