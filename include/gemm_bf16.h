@@ -106,13 +106,24 @@ typedef enum gemm_bf16_option {
     GEMM_BF16_OPT_STAGE_GROUP = 12,  /* ring stages released per MMA commit (WS only): 1 = every
                                         k-block; 2 = stages pair up behind one "empty" barrier
                                         (the ring depth must then be even); 0 (default) = 1 */
-    GEMM_BF16_OPT_STREAM_K = 13,     /* 1 (default): in the persistent WS kernel, when there is at
-                                        least one whole wave of tiles, the tiles that would form a
-                                        partial last wave are split along k over all resident SM
-                                        (pairs) -- each non-owner leaves an fp32
-                                        partial in a handle-owned workspace (128 KiB per CTA,
-                                        allocated by plan) that the owner of the tile's first
-                                        k-block adds before storing; 0: every tile runs whole */
+    GEMM_BF16_OPT_STREAM_K = 13,     /* Splitting tiles along k in the persistent WS kernel.  A
+                                        non-owner part of a split tile leaves an fp32 partial in a
+                                        handle-owned workspace (128 KiB per CTA and part, allocated
+                                        by plan) that the owner of the tile's first k-block adds
+                                        before storing.
+                                        1 (default): with at least one whole wave of tiles, the
+                                        tiles that would form a partial last wave are split over
+                                        all resident SM (pairs); with fewer tiles T than resident
+                                        SM (pairs) C, every tile may be split at one k-block H:
+                                        SM (pair) t computes [0, H) of tile t and n <= C - T others
+                                        share the tails [H, KB), with n and H picked by a cost
+                                        model measured on GB300 (the split is taken only when it
+                                        beats whole tiles by a margin; plan_info.sk_head reports it);
+                                        2: the partial-last-wave split only;
+                                        3: as 1, but every problem with fewer tiles than SM (pairs)
+                                        is split over all of them, whatever the cost (for tests
+                                        and measurements);
+                                        0: every tile runs whole */
     GEMM_BF16_OPT_PDL = 14,           /* 1 (default): launch with programmatic stream serialization,
                                         so the kernel's prologue (barrier set-up, tensor-memory
                                         allocation) overlaps the previous kernel on the stream; every
@@ -180,6 +191,8 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t packed_ld;            /* their pitch in elements (K rounded up to 64); 0 = none */
     int32_t k_order;              /* 0 = ascending, 1 = alternating */
     int32_t serpentine;           /* 1 = odd tile bands walk right to left */
+    int32_t sk_head;              /* > 0: every tile split at this k-block (head/tail stream-K) */
+    int32_t sk_slots;             /* fp32 partial slots (128 x 256 each) the workspace holds */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's

@@ -96,3 +96,15 @@ def test_create_without_a_usable_gpu_fails_cleanly(lib):
     st, h = binding.gemm_bf16_create(0)
     assert st in (binding.ERR_CUDA, binding.ERR_UNSUPPORTED)
     assert not h.value
+
+
+def test_plan_info_struct_matches_the_header():
+    # the binding's ctypes mirror of gemm_bf16_plan_info_t: same fields, order and types
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct gemm_bf16_plan_info_s \{(.*?)\} gemm_bf16_plan_info_t;", text, re.S).group(1)
+    fields = re.findall(r"^\s*(int32_t|int64_t)\s+(\w+);", body, re.M)
+    ctypes_of = {"int32_t": "c_int", "int64_t": "c_long"}
+    got = [(name, t.__name__) for name, t in binding.PlanInfo._fields_]
+    assert [n for n, _ in got] == [n for _, n in fields]
+    for (name, tname), (ctype, _) in zip(got, fields):
+        assert tname in (ctypes_of[ctype], "c_" + ctype.replace("_t", "")), (name, tname, ctype)

@@ -320,6 +320,132 @@ def test_stream_k_random_inputs_and_repeated_launches():
     assert torch.equal(outs[1].cpu().float(), (outs[0].cpu().float() * 2))
 
 
+# Fewer tiles than SM (pairs): every tile is split at the same k-block; the
+# owner computes the head and adds the partials of the tails, which the other
+# SM (pairs) share.  stream_k = 3 takes the split whatever the planner's cost
+# model says.  Shapes (with the cta_group = 2 / 1 tile counts T and cluster
+# counts C that max_ctas gives):
+HEAD_TAIL = [
+    (512, 512, 8192, 12),    # T = 4 / 8 on C = 6 / 12: a tail range holds two whole tails
+    (600, 700, 8200, 20),    # ragged edges and a k tail of 8 (T = 9 / 15, C = 10 / 20)
+    (256, 512, 8192, 16),    # T = 2 / 4 on C = 8 / 16: each tail split over three ranges
+    (1792, 256, 8192, 16),   # T = 7 / 14 on C = 8 / 16: one range holds seven tails
+]
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("M,N,K,max_ctas", HEAD_TAIL)
+def test_stream_k_head_tail_exact(cta_group, M, N, K, max_ctas):
+    A, B = inputs.make_problem(M, N, K, "int2", seed=M + N + K)
+    with binding.Gemm(0, cta_group=cta_group, max_ctas=max_ctas, stream_k=3) as g:
+        info = g.plan(M, N, K)
+    T, KB = info["tiles"], info["k_blocks"]
+    C = info["grid_ctas"] // cta_group
+    assert T < C == max_ctas // cta_group and info["sk_tiles"] == T
+    # tails are reckoned slower than heads, so a head is at least the even share
+    assert -(-T * KB // C) <= info["sk_head"] < KB
+    assert info["sk_slots"] >= (C - T) * cta_group
+    D = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stream_k=3)
+    check(D, A, B, M, N, K, exact=True)
+    # whole tiles (stream_k = 0) and the partial-wave-only setting (2, which
+    # leaves these tiles whole) give the same bits
+    for sk in (0, 2):
+        with binding.Gemm(0, cta_group=cta_group, max_ctas=max_ctas, stream_k=sk) as g:
+            assert g.plan(M, N, K)["sk_head"] == 0
+        D0 = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stream_k=sk)
+        assert torch.equal(D.view(torch.int16), D0.view(torch.int16))
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("sched", SCHEDULES)
+def test_schedules_with_head_tail_split(cta_group, sched):
+    M, N, K, max_ctas = 600, 700, 8200, 20
+    A, B = inputs.make_problem(M, N, K, "int2", seed=41)
+    with binding.Gemm(0, cta_group=cta_group, max_ctas=max_ctas, stream_k=3, **sched) as g:
+        assert g.plan(M, N, K)["sk_head"] > 0
+    D = run_gpu(A, B, M, N, K, cta_group=cta_group, max_ctas=max_ctas, stream_k=3, **sched)
+    check(D, A, B, M, N, K, exact=True)
+
+
+def test_head_tail_random_inputs_repeated_launches_and_full_grid():
+    # 2048 x 2048 x 32768 on the whole GPU (64 SM-pair tiles): launches on one
+    # handle reuse every partial slot, each with its own epoch
+    M, N, K = 2048, 2048, 32768
+    A, B = inputs.make_problem(M, N, K, "normal", seed=4)
+    A[:, ::97] *= 0.5  # not the longk workload's exact values
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    outs = []
+    with binding.Gemm(0) as g:
+        info = g.plan(M, N, K)
+        assert info["sk_head"] > 0 and info["sk_tiles"] == info["tiles"]
+        for i in range(3):
+            D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            g.run(dA if i != 1 else dA * 2, dB, D)
+            outs.append(D)
+        assert g.device_status()[0] == binding.OK
+    torch.cuda.synchronize()
+    rows = sample_rows(M, extra=8)
+    check(outs[0].cpu(), A, B, M, N, K, rows=rows)
+    assert torch.equal(outs[2].view(torch.int16), outs[0].view(torch.int16))
+    assert torch.equal(outs[1].cpu().float(), (outs[0].cpu().float() * 2))
+
+
+@pytest.mark.parametrize("M,N,K,split", [
+    (2048, 2048, 32768, True),    # 64 tiles, long k: the split pays (measured)
+    (1024, 1024, 32768, True),    # 16 tiles
+    (512, 512, 16384, True),      # 4 tiles
+    (1024, 1024, 4096, True),     # 16 tiles of 64 k-blocks
+    (2048, 2048, 8192, False),    # 64 tiles, short tails: the fixed cost of a split wins
+    (256, 256, 256, False),
+    (4096, 4096, 4096, False),    # more tiles than SM pairs: the partial-wave split instead
+])
+def test_head_tail_automatic_choice(M, N, K, split):
+    with binding.Gemm(0) as g:
+        info = g.plan(M, N, K)
+    assert (info["sk_head"] > 0) == split, info
+    if split:
+        assert info["grid_ctas"] // info["cta_group"] > info["tiles"] == info["sk_tiles"]
+    elif info["tiles"] * info["cta_group"] < info["num_sms"]:
+        assert info["sk_tiles"] == 0 and info["grid_ctas"] == info["tiles"] * info["cta_group"]
+
+
+def test_head_tail_fused_epilogue_exact():
+    M, N, K, max_ctas = 600, 520, 8192, 20
+    A, B = inputs.make_problem(M, N, K, "int2", seed=43)
+    g = torch.Generator().manual_seed(44)
+    C = inputs.make_operand(M, N, None, "int2", g)
+    bias = inputs.make_operand(1, N, None, "int2", g).reshape(-1)
+    with binding.Gemm(0, max_ctas=max_ctas, stream_k=3) as h:
+        assert h.plan(M, N, K)["sk_head"] > 0
+    D = run_fused_gpu(A, B, M, N, K, C=C, bias=bias, alpha=2.0, beta=-3.0, max_ctas=max_ctas, stream_k=3)
+    _, refbf = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 2.0, -3.0, C=inputs.bits(C),
+                                      bias=inputs.bits(bias))
+    assert np.array_equal(inputs.bits(D), refbf)
+
+
+def test_head_tail_watchdog_timeout_then_exact():
+    # a skipped load stalls a tail range; its owner's wait for the partial is
+    # bounded too, and the next launch on the handle (a new epoch) is exact
+    M, N, K, max_ctas = 512, 512, 8192, 12
+    A, B = inputs.make_problem(M, N, K, "int2", seed=45)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0, watchdog_ns=20_000_000, fault_skip_load=5, max_ctas=max_ctas, stream_k=3) as g:
+        assert g.plan(M, N, K)["sk_head"] > 0
+        g.run(dA, dB, dD)
+        st, detail = g.device_status()
+        assert st == binding.ERR_DEVICE_TIMEOUT and detail & 0x80000000
+        g.set_option("fault_skip_load", -1)
+        g.plan(M, N, K)
+        for _ in range(2):
+            dD.fill_(3.0)
+            g.run(dA, dB, dD)
+            assert g.device_status()[0] == binding.OK
+            check(dD.cpu(), A, B, M, N, K, exact=True)
+
+
 @pytest.mark.parametrize("N,epilogue,ldd", [
     (517, 0, 520), (517, 1, 520), (517, 2, 520), (517, 0, 523), (517, 2, 528), (517, 1, 600),
     (512, 1, 520), (520, 1, 600), (64, 1, 72), (1, 2, 1), (7, 0, 8)])

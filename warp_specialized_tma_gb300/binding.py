@@ -104,6 +104,8 @@ class PlanInfo(ctypes.Structure):
         ("packed_ld", ctypes.c_int32),
         ("k_order", ctypes.c_int32),
         ("serpentine", ctypes.c_int32),
+        ("sk_head", ctypes.c_int32),
+        ("sk_slots", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -8,11 +8,13 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "gemm_kernels.h"
 
@@ -32,6 +34,10 @@ struct Plan {
     int acc_buffers = 2;
     int stage_group = 1;
     int sk_tiles = 0;
+    int sk_head = 0;        // > 0: head/tail stream-K (fewer tiles than clusters)
+    int sk_pieces = 0;      // workspace slots per contributing cluster
+    int64_t sk_units = 0;   // units divided among the clusters' ranges
+    size_t sk_slots = 0;    // partial slots (per CTA) the workspace must hold
     int setmaxnreg = 0;
     int stages = 0;
     int raster_group = 8;
@@ -125,7 +131,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_WATCHDOG_NS: return v >= 1000 && v <= 600LL * 1000000000LL;
     case GEMM_BF16_OPT_FAULT_SKIP_LOAD: return v >= -1 && v <= kMaxDim;
     case GEMM_BF16_OPT_STAGE_GROUP: return v >= 0 && v <= 2;
-    case GEMM_BF16_OPT_STREAM_K: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_STREAM_K: return v >= 0 && v <= 3;
     case GEMM_BF16_OPT_PDL: return v == 0 || v == 1;
     case GEMM_BF16_OPT_EPI_SCHEDULE: return v == 0 || v == 1;
     case GEMM_BF16_OPT_SCHEDULER: return v == 0 || v == 1;
@@ -134,6 +140,62 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_SERPENTINE: return v == 0 || v == 1;
     default: return false;
     }
+}
+
+// Head/tail stream-K for T tiles of KB k-blocks on up to C clusters (T < C):
+// cluster t < T computes k-blocks [0, H) of tile t, and n more clusters share
+// the T * (KB - H) tail k-blocks in contiguous ranges.  The constants are
+// measured on GB300 (in k-blocks of one SM pair's MMA time, ~0.3 us each):
+//  - a tail k-block runs at kTailWeight % of a head k-block's time (the tails'
+//    operand slices have fewer concurrent readers, so more come from DRAM),
+//    and H = ceil(w*T*KB / (n + w*T)) balances the two;
+//  - an owner folds each tail's fp32 partial (128 KiB per CTA, from L2) into
+//    a spare tensor-memory accumulator as it arrives: kPartialCost per tail;
+//  - storing a partial, raising its flag and the owner's final pass cost a
+//    fixed kMinSaving that the split must save first.
+// The n with the least H + kPartialCost * (most tails in one tile) is chosen,
+// and the split is taken when that beats a whole tile by >= kMinSaving.
+struct HeadTail {
+    int64_t head = 0, n = 0, units = 0, pieces = 0;
+};
+
+bool choose_head_tail(int64_t T, int64_t KB, int64_t C, bool forced, HeadTail *out)
+{
+    constexpr int64_t kPartialCost = 6;
+    constexpr int64_t kTailWeight = 130;
+    constexpr int64_t kMinSaving = 24;
+    // forced: every cluster takes part, whatever the cost
+    int64_t best_cost = forced ? INT64_MAX : KB - kMinSaving + 1;
+    bool found = false;
+    std::vector<int32_t> ranges_in_tile((size_t)T);
+    for (int64_t n = forced ? C - T : 1; n <= C - T; ++n) {
+        const int64_t den = 100 * n + kTailWeight * T;
+        const int64_t head = (kTailWeight * T * KB + den - 1) / den;
+        const int64_t L = KB - head;
+        if (L < 1)
+            continue;
+        const int64_t U = T * L;
+        std::fill(ranges_in_tile.begin(), ranges_in_tile.end(), 0);
+        int64_t pieces = 1, most = 0;
+        for (int64_t j = 0; j < n; ++j) {
+            const int64_t b = j * U / n, e = (j + 1) * U / n;
+            if (e <= b)
+                continue;
+            pieces = std::max<int64_t>(pieces, (e - 1) / L - b / L + 1);
+            for (int64_t t = b / L; t <= (e - 1) / L; ++t)
+                most = std::max<int64_t>(most, ++ranges_in_tile[(size_t)t]);
+        }
+        const int64_t cost = head + kPartialCost * most;
+        if (cost < best_cost) {
+            best_cost = cost;
+            out->head = head;
+            out->n = n;
+            out->units = U;
+            out->pieces = pieces;
+            found = true;
+        }
+    }
+    return found;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -409,6 +471,10 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
     // grid
     const int64_t max_ctas = h->opt[GEMM_BF16_OPT_MAX_CTAS];
     pl.sk_tiles = 0;
+    pl.sk_head = 0;
+    pl.sk_pieces = 0;
+    pl.sk_units = 0;
+    pl.sk_slots = 0;
     if (!ws || !pl.persistent) {
         pl.grid_ctas = (int)(pl.tiles * cg);
     } else {
@@ -446,22 +512,41 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         // gets >= 4 k-blocks of the split work.
         const int64_t clusters = slots / cg;
         const int64_t rem = pl.tiles % clusters;
-        if (h->opt[GEMM_BF16_OPT_STREAM_K] && pl.tiles >= clusters && rem != 0 &&
-            rem * pl.num_k_blocks >= 4 * clusters) {
+        const int64_t sk_opt = h->opt[GEMM_BF16_OPT_STREAM_K];
+        const int64_t KB = pl.num_k_blocks;
+        if (sk_opt && pl.tiles >= clusters && rem != 0 && rem * KB >= 4 * clusters) {
             pl.sk_tiles = (int)rem;
+            pl.sk_units = rem * KB;
+            pl.sk_pieces = 1;
+            pl.sk_slots = (size_t)(clusters * cg);
             pl.grid_ctas = (int)(clusters * cg);
+        } else if ((sk_opt == 1 || sk_opt == 3) && pl.tiles < clusters) {
+            // Head/tail form: every tile is split at the same k-block H, so the
+            // tiles' owners all start at k-block 0 and walk k in step (the A and
+            // B panels they share are read from DRAM once, as with whole tiles),
+            // while n of the clusters that would idle share the tails.
+            HeadTail ht;
+            if (choose_head_tail(pl.tiles, KB, clusters, sk_opt == 3, &ht)) {
+                pl.sk_tiles = (int)pl.tiles;
+                pl.sk_head = (int)ht.head;
+                pl.sk_units = ht.units;
+                pl.sk_pieces = (int)ht.pieces;
+                pl.sk_slots = (size_t)(ht.n * ht.pieces * cg);
+                pl.grid_ctas = (int)((pl.tiles + ht.n) * cg);
+            }
         }
     }
     if (!ws && max_ctas > 0)
         return GEMM_BF16_ERR_UNSUPPORTED;  // one tile per CTA: the grid is fixed by the problem
-    if (pl.sk_tiles > 0 && (size_t)pl.grid_ctas > h->ws_slots) {
-        // one partial slot (128 x 256 fp32) and one flag per CTA; flags start at 0
-        // and every launch waits for its own epoch, so they are never reset
+    if (pl.sk_tiles > 0 && pl.sk_slots > h->ws_slots) {
+        // one partial slot (128 x 256 fp32) and one flag per contributor CTA and
+        // piece; flags start at 0 and every launch waits for its own epoch, so
+        // they are never reset
         float *nws = nullptr;
         uint32_t *nflags = nullptr;
-        if (cudaMalloc(&nws, (size_t)pl.grid_ctas * kPartialFloats * sizeof(float)) != cudaSuccess ||
-            cudaMalloc(&nflags, (size_t)pl.grid_ctas * sizeof(uint32_t)) != cudaSuccess ||
-            cudaMemset(nflags, 0, (size_t)pl.grid_ctas * sizeof(uint32_t)) != cudaSuccess) {
+        if (cudaMalloc(&nws, pl.sk_slots * kPartialFloats * sizeof(float)) != cudaSuccess ||
+            cudaMalloc(&nflags, pl.sk_slots * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(nflags, 0, pl.sk_slots * sizeof(uint32_t)) != cudaSuccess) {
             cudaGetLastError();
             if (nws)
                 cudaFree(nws);
@@ -475,7 +560,7 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
             cudaFree(h->ws_flags);
         h->ws = nws;
         h->ws_flags = nflags;
-        h->ws_slots = (size_t)pl.grid_ctas;
+        h->ws_slots = pl.sk_slots;
     }
     // Operand repacking: a row pitch that is not a multiple of 128 bytes makes
     // every TMA box row straddle two L2 lines (~28% slower GEMM, measured).  A
@@ -532,6 +617,8 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->setmaxnreg = p.setmaxnreg;
     info->stage_group = p.stage_group;
     info->sk_tiles = p.sk_tiles;
+    info->sk_head = p.sk_head;
+    info->sk_slots = (int32_t)p.sk_slots;
     info->tile_m = kBlockM * p.cta_group;
     info->tile_n = kBlockN;
     info->tile_k = kBlockK;
@@ -643,7 +730,9 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     prm.err = h->d_err;
     prm.watchdog_ns = pl.watchdog_ns;
     prm.sk_tiles = pl.sk_tiles;
-    prm.sk_units = (int64_t)pl.sk_tiles * pl.num_k_blocks;
+    prm.sk_units = pl.sk_units;
+    prm.sk_head = pl.sk_head;
+    prm.sk_pieces = pl.sk_pieces;
     prm.workspace = pl.sk_tiles ? h->ws : nullptr;
     prm.flags = pl.sk_tiles ? h->ws_flags : nullptr;
     if (++h->epoch == 0)

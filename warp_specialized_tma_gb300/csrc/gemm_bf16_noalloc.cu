@@ -208,6 +208,8 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     prm.sk_tiles = 0;  // stream-K needs a partials workspace, which this entry point does not have
     prm.epoch = 1;
     prm.sk_units = 0;
+    prm.sk_head = 0;
+    prm.sk_pieces = 0;
     prm.workspace = nullptr;
     prm.flags = nullptr;
     prm.C = nullptr;

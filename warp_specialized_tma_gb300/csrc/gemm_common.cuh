@@ -39,48 +39,120 @@ struct WorkItem {
     int32_t kb1;
 };
 
-// First stream-K unit of cluster c (unit u = k-block u % KB of tile u / KB):
-// the sk_units are split into C contiguous, near-equal ranges.
-__device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int32_t c, int32_t C)
+// Stream-K units.  The split tiles' k-blocks that are shared out form a line of
+// sk_units units: unit u is k-block sk_head + u % L of tile u / L, with
+// L = num_k_blocks - sk_head units per tile.  The line is cut into n
+// contiguous, near-equal ranges, range j = [sk_begin(j), sk_begin(j + 1)):
+//   sk_head == 0: L = KB, n = C, cluster c takes range c;
+//   sk_head  > 0: n = C - sk_tiles, cluster sk_tiles + j takes range j, and
+//                 cluster t < sk_tiles computes the head [0, sk_head) of tile t.
+// A contributor (an item that does not start at k-block 0) leaves its fp32
+// partial in workspace slot sk_slot(); the item that holds k-block 0 (the
+// owner) adds every contributor's partial before it stores the tile.
+__device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int32_t j, int32_t n)
 {
-    return (int64_t)c * p.sk_units / C;
+    return (int64_t)j * p.sk_units / n;
 }
 
-// A cluster's work, in order: its contiguous share of the stream-K units
-// (tiles [0, sk_tiles), split along k), then the whole tiles sk_tiles + c,
-// sk_tiles + c + C, ...  Every role of the CTA walks the same sequence.
+__device__ __forceinline__ int32_t sk_ranges(const GemmParams &p, int32_t C)
+{
+    return p.sk_head > 0 ? C - p.sk_tiles : C;
+}
+
+// Slot of range j's partial of `tile` (its range starts at unit b).  With
+// sk_head == 0 a range contributes at most once, its first item; with
+// sk_head > 0 every item of a range is a contributor, one per tile.
+__device__ __forceinline__ int32_t sk_slot(const GemmParams &p, int32_t j, int64_t b, int32_t tile)
+{
+    if (p.sk_head == 0)
+        return j;
+    const int64_t L = p.num_k_blocks - p.sk_head;
+    return j * p.sk_pieces + (tile - (int32_t)(b / L));
+}
+
+// A cluster's work, in order: its stream-K items (its range of units, or the
+// head of its tile), then the whole tiles sk_tiles + c, sk_tiles + c + C, ...
+// Every role of the CTA walks the same sequence.
 struct WorkIter {
-    int64_t u, u_end, KB;
-    int32_t dp, C, T;
+    int64_t u, u_end, L;
+    int32_t koff, dp, C, T, KB;
 
     __device__ __forceinline__ void init(const GemmParams &p, int32_t cluster, int32_t nclusters)
     {
         KB = p.num_k_blocks;
         C = nclusters;
         T = p.num_tiles;
-        u = sk_begin(p, cluster, nclusters);
-        u_end = sk_begin(p, cluster + 1, nclusters);
         dp = p.sk_tiles + cluster;
+        if (p.sk_head > 0 && cluster < p.sk_tiles) {
+            L = p.num_k_blocks;
+            koff = 0;
+            u = (int64_t)cluster * L;
+            u_end = u + p.sk_head;
+        } else {
+            const int32_t j = p.sk_head > 0 ? cluster - p.sk_tiles : cluster;
+            const int32_t n = sk_ranges(p, nclusters);
+            L = p.num_k_blocks - p.sk_head;
+            koff = p.sk_head;
+            u = sk_begin(p, j, n);
+            u_end = sk_begin(p, j + 1, n);
+        }
     }
 
     __device__ __forceinline__ bool next(WorkItem &w)
     {
         if (u < u_end) {
-            const int64_t t = u / KB;
-            const int64_t k0 = u - t * KB;
-            const int64_t k1 = (k0 + (u_end - u) < KB) ? k0 + (u_end - u) : KB;
+            const int64_t t = u / L;
+            const int64_t k0 = u - t * L;
+            const int64_t k1 = (k0 + (u_end - u) < L) ? k0 + (u_end - u) : L;
             w.tile = (int32_t)t;
-            w.kb0 = (int32_t)k0;
-            w.kb1 = (int32_t)k1;
+            w.kb0 = koff + (int32_t)k0;
+            w.kb1 = koff + (int32_t)k1;
             u += k1 - k0;
             return true;
         }
         if (dp < T) {
             w.tile = dp;
             w.kb0 = 0;
-            w.kb1 = (int32_t)KB;
+            w.kb1 = KB;
             dp += C;
             return true;
+        }
+        return false;
+    }
+};
+
+// The contributors to split tile `tile`, whose owner is cluster `owner`: the
+// non-empty ranges that reach into the tile's units, in range order.  next()
+// gives each one's workspace slot.
+struct ContribIter {
+    int64_t lo, hi;
+    int32_t j, n, tile;
+
+    __device__ __forceinline__ void init(const GemmParams &p, int32_t tile_, int32_t owner, int32_t C)
+    {
+        tile = tile_;
+        n = sk_ranges(p, C);
+        const int64_t L = p.num_k_blocks - p.sk_head;
+        lo = (int64_t)tile * L;
+        hi = lo + L;
+        // sk_head == 0: the owner's own range holds unit lo, the later ones the
+        // rest.  sk_head > 0: no range before floor(tile * n / sk_tiles) ends
+        // after lo, since that range begins at or before lo.
+        j = p.sk_head > 0 ? (int32_t)((int64_t)tile * n / p.sk_tiles) : owner + 1;
+    }
+
+    __device__ __forceinline__ bool next(const GemmParams &p, int32_t &slot)
+    {
+        for (; j < n; ++j) {
+            const int64_t b = sk_begin(p, j, n);
+            if (b >= hi)
+                return false;
+            const int64_t e = sk_begin(p, j + 1, n);
+            if (e > b && e > lo) {
+                slot = sk_slot(p, j, b, tile);
+                ++j;
+                return true;
+            }
         }
         return false;
     }
@@ -232,6 +304,20 @@ __device__ __forceinline__ void partial_store(float *slot, int ew, int c, int la
     }
 }
 
+__device__ __forceinline__ void partial_load(float *slot, int ew, int c, int lane, uint32_t (&v0)[32],
+                                             uint32_t (&v1)[32])
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float4 f = __ldcg(partial_addr(slot, ew, c, j, lane));
+        uint32_t *v = j < 8 ? &v0[4 * j] : &v1[4 * (j - 8)];
+        v[0] = __float_as_uint(f.x);
+        v[1] = __float_as_uint(f.y);
+        v[2] = __float_as_uint(f.z);
+        v[3] = __float_as_uint(f.w);
+    }
+}
+
 __device__ __forceinline__ void partial_add(float *slot, int ew, int c, int lane, uint32_t (&v0)[32],
                                             uint32_t (&v1)[32])
 {
@@ -243,6 +329,22 @@ __device__ __forceinline__ void partial_add(float *slot, int ew, int c, int lane
         v[1] = __float_as_uint(__uint_as_float(v[1]) + f.y);
         v[2] = __float_as_uint(__uint_as_float(v[2]) + f.z);
         v[3] = __float_as_uint(__uint_as_float(v[3]) + f.w);
+    }
+}
+
+// v += the 32 fp32 columns of tensor memory at taddr (this warp's 32 lanes).
+__device__ __forceinline__ void tmem_add_32x32(uint32_t taddr, uint32_t (&v)[32])
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t t[16];
+        tmem_load_32x16(taddr + 16u * (uint32_t)h, t);
+        tmem_load_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            asm volatile("" : "+r"(t[i])::"memory");
+            v[16 * h + i] = __float_as_uint(__uint_as_float(v[16 * h + i]) + __uint_as_float(t[i]));
+        }
     }
 }
 

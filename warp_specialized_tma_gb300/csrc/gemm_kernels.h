@@ -42,13 +42,20 @@ struct GemmParams {
     void *D;
     uint32_t *err;          // device status word (0 = fine)
     uint64_t watchdog_ns;
-    // stream-K (WS only): tiles [0, sk_tiles) are split along k across all
-    // clusters, the other tiles are walked whole.  0 = off.
+    // stream-K (WS only): tiles [0, sk_tiles) are split along k, the other
+    // tiles are walked whole.  0 = off.  Two forms:
+    //   sk_head == 0 (partial last wave): the split tiles' (tile, k-block)
+    //     units are divided among all clusters;
+    //   sk_head  > 0 (fewer tiles than clusters, sk_tiles = num_tiles): cluster
+    //     t computes k-blocks [0, sk_head) of tile t, and the tails [sk_head, KB)
+    //     of every tile are divided among the remaining clusters.
     int32_t sk_tiles;
     uint32_t epoch;         // this launch's flag value (never 0)
-    int64_t sk_units;       // sk_tiles * num_k_blocks
-    float *workspace;       // partials: per (cluster, rank) 128 x 256 fp32 = kPartialFloats
-    uint32_t *flags;        // per (cluster, rank): == epoch once that partial is complete
+    int64_t sk_units;       // units divided among clusters: sk_tiles * (num_k_blocks - sk_head)
+    int32_t sk_head;
+    int32_t sk_pieces;      // workspace slots per contributing cluster (1 when sk_head == 0)
+    float *workspace;       // partials: per (slot, rank) 128 x 256 fp32 = kPartialFloats
+    uint32_t *flags;        // per (slot, rank): == epoch once that partial is complete
     // fused epilogue D = alpha * acc + beta * C + bias (when fused != 0)
     const void *C;          // bf16, row pitch ldc (may alias D with ldc == ldd)
     const void *bias;       // bf16 [N]

@@ -394,6 +394,49 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             WorkItem skip;
             wi.next(skip);
         }
+        // Head/tail stream-K owner (cooperative schedule): this cluster's only
+        // item is the head of tile cluster_id, accumulating in buffer 0, and
+        // buffer 1 stays free.  While the head's MMAs run, the epilogue warps
+        // fold each tail's partial into buffer 1 as soon as that tail raises its
+        // flag (the tails finish one after another), so after the last MMA the
+        // tile's epilogue adds one sum from tensor memory and at most the last
+        // tail's partial was read on the critical path.
+        const bool parked = p.sk_head > 0 && cluster_id < p.sk_tiles && !pingpong && p.acc_buffers == 2;
+        if (parked) {
+            const uint32_t spare = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kBlockN + col0);
+            ContribIter ci;
+            ci.init(p, cluster_id, cluster_id, num_clusters);
+            int32_t s2;
+            bool first = true;
+            while (ci.next(p, s2)) {
+                const int32_t slot2 = s2 * CG + (int32_t)rank;
+                if (!warp_wait_flag(ctl, p.flags + slot2, p.epoch, lane))
+                    break;
+#pragma unroll 1
+                for (int c = 0; c < nchunks; ++c) {
+                    const int32_t col = col0 + c * 64;
+                    const int pw = (col >> 7) * 4 + q;
+                    const int pc = (col >> 6) & 1;
+                    float *const part = p.workspace + (size_t)slot2 * kPartialFloats;
+                    uint32_t v0[32], v1[32];
+                    if (first) {
+                        partial_load(part, pw, pc, lane, v0, v1);
+                    } else {
+                        tmem_load_32x32(spare + (uint32_t)(c * 64), v0);
+                        tmem_load_32x32(spare + (uint32_t)(c * 64 + 32), v1);
+                        tmem_load_wait();
+                        reg_fence(v0);
+                        reg_fence(v1);
+                        partial_add(part, pw, pc, lane, v0, v1);
+                    }
+                    tmem_store_32x32(spare + (uint32_t)(c * 64), v0);
+                    tmem_store_32x32(spare + (uint32_t)(c * 64 + 32), v1);
+                }
+                // the next tail's pass reads what this one stored
+                tmem_store_wait();
+                first = false;
+            }
+        }
         for (;;) {
             // One thread per group finds the next item and polls the accumulator
             // barrier, then posts both; the other warps sleep on a named barrier
@@ -442,11 +485,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             // A stream-K item that does not start at k-block 0 is a contributor: it
             // leaves its fp32 partial for the tile's owner.  The item holding
             // k-block 0 of a split tile is the owner: it adds every contributor's
-            // partial before storing.  Each cluster contributes at most once (its
-            // first item), so its workspace slot is its own.
+            // partial before storing.
             const bool contributor = w.kb0 > 0;
             const bool owner = w.kb0 == 0 && w.kb1 < KB;
-            const int32_t slot_id = cluster_id * CG + (int32_t)rank;
+            int32_t slot_id = 0;
+            if (contributor) {
+                const int32_t j = p.sk_head > 0 ? cluster_id - p.sk_tiles : cluster_id;
+                slot_id = sk_slot(p, j, sk_begin(p, j, sk_ranges(p, num_clusters)), w.tile) * CG + (int32_t)rank;
+            }
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBlockN + col0);
 #pragma unroll 1
             for (int c = 0; c < nchunks; ++c) {
@@ -461,6 +507,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tmem_load_wait();
                 reg_fence(v0);
                 reg_fence(v1);
+                if (owner && parked) {
+                    // the tails' summed partials, parked in the other accumulator
+                    const uint32_t spare = tbase + (uint32_t)kBlockN + (uint32_t)(c * 64);
+                    tmem_add_32x32(spare, v0);
+                    tmem_add_32x32(spare + 32u, v1);
+                }
                 if (c == nchunks - 1) {
                     // every read of this accumulator is done: hand it back to the MMA warp
                     tc_fence_before_sync();
@@ -476,17 +528,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     partial_store(p.workspace + (size_t)slot_id * kPartialFloats, pw, pc, lane, v0, v1);
                     continue;
                 }
-                if (owner) {
-                    // contributors: the next clusters whose (non-empty) ranges start
-                    // inside this tile
-                    const int64_t tile_end = (int64_t)(w.tile + 1) * KB;
-                    for (int32_t c2 = cluster_id + 1; c2 < num_clusters; ++c2) {
-                        const int64_t b2 = sk_begin(p, c2, num_clusters);
-                        if (b2 >= tile_end)
-                            break;
-                        if (sk_begin(p, c2 + 1, num_clusters) == b2)
-                            continue;
-                        const int32_t slot2 = c2 * CG + (int32_t)rank;
+                if (owner && !parked) {
+                    ContribIter ci;
+                    ci.init(p, w.tile, cluster_id, num_clusters);
+                    int32_t s2;
+                    while (ci.next(p, s2)) {
+                        const int32_t slot2 = s2 * CG + (int32_t)rank;
                         if (c == 0 && !warp_wait_flag(ctl, p.flags + slot2, p.epoch, lane))
                             break;
                         partial_add(p.workspace + (size_t)slot2 * kPartialFloats, pw, pc, lane, v0, v1);
