@@ -12,11 +12,13 @@ stage ring with __syncthreads up to the default kernel:
   +tmem2      two TMEM accumulators: the epilogue overlaps the next tile
   +setmaxnreg producer warps give registers to the epilogue warps
   +2cta       an SM pair per 256x256 tile (cta_group::2)
-  +streamk    the partial last wave of tiles split along k
+  +streamk    tiles split along k: the partial last wave, or, with fewer tiles
+              than SM pairs, every tile's tail taken by an idle SM pair
   +k-alt      consecutive whole tiles walk k in alternating directions
   +serpentine odd tile bands walk their columns right to left (the default)
 
-With --schedules the default kernel is compared with its schedule options
+With --shape M N K the workload's distribution and seed are drawn at another
+shape.  With --schedules the default kernel is compared with its schedule options
 instead: the ping-pong epilogue, the dynamic tile counter, and both.  With
 --variant NAME:OPT=V,OPT=V (repeatable) any named option sets are compared,
 e.g. --variant aligned:repack=0 --variant unaligned:repack=2.
@@ -63,6 +65,8 @@ SCHEDULE_RUNGS = [
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--workload", default="cube8192", choices=list(inputs.WORKLOADS))
+    ap.add_argument("--shape", type=int, nargs=3, metavar=("M", "N", "K"),
+                    help="override the workload's shape (its distribution and seed are kept)")
     ap.add_argument("--rounds", type=int, default=5)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--device", type=int, default=0)
@@ -84,8 +88,8 @@ def main(argv=None) -> int:
     torch.cuda.set_device(args.device)
     dev = torch.device("cuda", args.device)
     w = inputs.WORKLOADS[args.workload]
-    M, N, K = w["M"], w["N"], w["K"]
-    A, B = inputs.make_workload(args.workload)
+    M, N, K = args.shape if args.shape else (w["M"], w["N"], w["K"])
+    A, B = inputs.make_problem(M, N, K, w["dist"], w["seed"])
     dA, dB = A.to(dev), B.to(dev)
     dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     handles = []
@@ -120,10 +124,11 @@ def main(argv=None) -> int:
         st, detail = g.device_status()
         rc |= st != binding.OK
         best, med = min(times[name]), statistics.median(times[name])
-        print(json.dumps({"workload": args.workload, "rung": name, "best_ms": round(best, 4),
+        print(json.dumps({"workload": args.workload, "shape": [M, N, K], "rung": name, "best_ms": round(best, 4),
                           "median_ms": round(med, 4), "tflops_best": round(flops / best / 1e9, 1),
                           "tflops_median": round(flops / med / 1e9, 1), "grid": info["grid_ctas"],
-                          "stages": info["stages"], "sk_tiles": info["sk_tiles"], "repack": info["repack"],
+                          "stages": info["stages"], "sk_tiles": info["sk_tiles"], "sk_head": info["sk_head"],
+                          "repack": info["repack"],
                           "status": st}))
         g.close()
     return rc
