@@ -143,54 +143,76 @@ bool option_in_range(int key, int64_t v)
 }
 
 // Head/tail stream-K for T tiles of KB k-blocks on up to C clusters (T < C):
-// cluster t < T computes k-blocks [0, H) of tile t, and n more clusters share
-// the T * (KB - H) tail k-blocks in contiguous ranges.  The constants are
-// measured on GB300 (in k-blocks of one SM pair's MMA time, ~0.3 us each):
-//  - a tail k-block runs at kTailWeight % of a head k-block's time (the tails'
-//    operand slices have fewer concurrent readers, so more come from DRAM),
-//    and H = ceil(w*T*KB / (n + w*T)) balances the two;
-//  - an owner folds each tail's fp32 partial (128 KiB per CTA, from L2) into
-//    a spare tensor-memory accumulator as it arrives: kPartialCost per tail;
-//  - storing a partial, raising its flag and the owner's final pass cost a
-//    fixed kMinSaving that the split must save first.
-// The n with the least H + kPartialCost * (most tails in one tile) is chosen,
-// and the split is taken when that beats a whole tile by >= kMinSaving.
+// cluster t < T computes k-blocks [0, H) of tile t (the head) and owns the
+// tile, and n more clusters share the T * (KB - H) tail k-blocks in
+// contiguous ranges of `share` k-blocks.  Times are in k-blocks of one SM
+// pair's MMA time (~0.3 us); the constants were measured on GB300 with
+// clock-stamped timelines of the kernel:
+//  - a tail k-block takes kTailWeight % of a head k-block (tail slices have
+//    fewer concurrent readers, so more of them come from DRAM);
+//  - after its last MMA a tail range needs kTailEnd to store its fp32
+//    partial (128 KiB per CTA) and raise its flag;
+//  - an owner folds each partial into a spare tensor-memory accumulator as it
+//    arrives; one that arrives at the end costs it kFold;
+// so the owner's epilogue can start at H when
+//   H >= w * share + kTailEnd + kFold * (most ranges reaching into one tile),
+// which fixes H for each n.  A range that covers more than two tiles stores a
+// partial per tile while it computes the next; with tails shorter than
+// kMinPiece k-blocks those stores hold its MMAs back (2048 x 2048 x 8192,
+// 14-k-block tails: 18% slower than whole tiles), so such layouts are not
+// used.  The n with the least H is chosen, and the split is taken when H beats
+// a whole tile by >= kMinSaving.
 struct HeadTail {
     int64_t head = 0, n = 0, units = 0, pieces = 0;
 };
 
+// For tails of L k-blocks cut into n ranges: the most ranges that reach into
+// one tile, and the most tiles one range reaches into.
+void tail_layout(int64_t T, int64_t L, int64_t n, std::vector<int32_t> &cnt, int64_t *most, int64_t *pieces)
+{
+    const int64_t U = T * L;
+    std::fill(cnt.begin(), cnt.end(), 0);
+    *most = 0;
+    *pieces = 1;
+    for (int64_t j = 0; j < n; ++j) {
+        const int64_t b = j * U / n, e = (j + 1) * U / n;
+        if (e <= b)
+            continue;
+        *pieces = std::max<int64_t>(*pieces, (e - 1) / L - b / L + 1);
+        for (int64_t t = b / L; t <= (e - 1) / L; ++t)
+            *most = std::max<int64_t>(*most, ++cnt[(size_t)t]);
+    }
+}
+
 bool choose_head_tail(int64_t T, int64_t KB, int64_t C, bool forced, HeadTail *out)
 {
-    constexpr int64_t kPartialCost = 6;
-    constexpr int64_t kTailWeight = 130;
-    constexpr int64_t kMinSaving = 24;
-    // forced: every cluster takes part, whatever the cost
-    int64_t best_cost = forced ? INT64_MAX : KB - kMinSaving + 1;
+    constexpr int64_t kTailWeight = 125;
+    constexpr int64_t kTailEnd = 15;
+    constexpr int64_t kFold = 6;
+    constexpr int64_t kMinPiece = 24;
+    constexpr int64_t kMinSaving = 8;
+    // forced: every cluster takes part, whatever the gain
+    int64_t best = forced ? INT64_MAX : KB - kMinSaving + 1;
     bool found = false;
-    std::vector<int32_t> ranges_in_tile((size_t)T);
+    std::vector<int32_t> cnt((size_t)T);
     for (int64_t n = forced ? C - T : 1; n <= C - T; ++n) {
         const int64_t den = 100 * n + kTailWeight * T;
-        const int64_t head = (kTailWeight * T * KB + den - 1) / den;
-        const int64_t L = KB - head;
-        if (L < 1)
+        // balance without the end costs first, to count the ranges per tile
+        const int64_t h0 = (kTailWeight * T * KB + den - 1) / den;
+        if (h0 >= KB)
             continue;
-        const int64_t U = T * L;
-        std::fill(ranges_in_tile.begin(), ranges_in_tile.end(), 0);
-        int64_t pieces = 1, most = 0;
-        for (int64_t j = 0; j < n; ++j) {
-            const int64_t b = j * U / n, e = (j + 1) * U / n;
-            if (e <= b)
-                continue;
-            pieces = std::max<int64_t>(pieces, (e - 1) / L - b / L + 1);
-            for (int64_t t = b / L; t <= (e - 1) / L; ++t)
-                most = std::max<int64_t>(most, ++ranges_in_tile[(size_t)t]);
-        }
-        const int64_t cost = head + kPartialCost * most;
-        if (cost < best_cost) {
-            best_cost = cost;
+        int64_t most, pieces;
+        tail_layout(T, KB - h0, n, cnt, &most, &pieces);
+        int64_t head = (kTailWeight * T * KB + 100 * n * (kTailEnd + kFold * most) + den - 1) / den;
+        head = std::min<int64_t>(head, KB - 1);
+        tail_layout(T, KB - head, n, cnt, &most, &pieces);
+        if (!forced && pieces > 2 && KB - head < kMinPiece)
+            continue;
+        if (head < best) {
+            best = head;
             out->head = head;
             out->n = n;
-            out->units = U;
+            out->units = T * (KB - head);
             out->pieces = pieces;
             found = true;
         }
