@@ -1,5 +1,7 @@
 // Pieces shared by the warp-specialised kernel and the non-specialised
 // ablation kernels: the output-tile order and the epilogue store of one chunk.
+// The tile order and the stream-K work split are also host functions, so
+// that tests can check them on the CPU.
 #pragma once
 
 #include "gemm_kernels.h"
@@ -18,14 +20,14 @@ struct TileCoord {
 // row-major order.  With p.serpentine, odd bands walk their columns right to
 // left: the first wave of a band then needs the B panels the last wave of the
 // previous band has just read.
-__device__ __forceinline__ TileCoord tile_coord(int32_t t, const GemmParams &p)
+__host__ __device__ __forceinline__ TileCoord tile_coord(int32_t t, const GemmParams &p)
 {
     if (p.raster_group <= 0)
         return {t / p.num_n_blocks, t % p.num_n_blocks};
     const int32_t span = p.raster_group * p.num_n_blocks;
     const int32_t band = t / span;
     const int32_t first = band * p.raster_group;
-    const int32_t rows = min(p.num_m_blocks - first, p.raster_group);
+    const int32_t rows = p.num_m_blocks - first < p.raster_group ? p.num_m_blocks - first : p.raster_group;
     const int32_t r = t - band * span;
     const int32_t col = r / rows;
     return {first + r % rows, (p.serpentine && (band & 1)) ? p.num_n_blocks - 1 - col : col};
@@ -49,12 +51,12 @@ struct WorkItem {
 // A contributor (an item that does not start at k-block 0) leaves its fp32
 // partial in workspace slot sk_slot(); the item that holds k-block 0 (the
 // owner) adds every contributor's partial before it stores the tile.
-__device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int32_t j, int32_t n)
+__host__ __device__ __forceinline__ int64_t sk_begin(const GemmParams &p, int32_t j, int32_t n)
 {
     return (int64_t)j * p.sk_units / n;
 }
 
-__device__ __forceinline__ int32_t sk_ranges(const GemmParams &p, int32_t C)
+__host__ __device__ __forceinline__ int32_t sk_ranges(const GemmParams &p, int32_t C)
 {
     return p.sk_head > 0 ? C - p.sk_tiles : C;
 }
@@ -62,7 +64,7 @@ __device__ __forceinline__ int32_t sk_ranges(const GemmParams &p, int32_t C)
 // Slot of range j's partial of `tile` (its range starts at unit b).  With
 // sk_head == 0 a range contributes at most once, its first item; with
 // sk_head > 0 every item of a range is a contributor, one per tile.
-__device__ __forceinline__ int32_t sk_slot(const GemmParams &p, int32_t j, int64_t b, int32_t tile)
+__host__ __device__ __forceinline__ int32_t sk_slot(const GemmParams &p, int32_t j, int64_t b, int32_t tile)
 {
     if (p.sk_head == 0)
         return j;
@@ -77,7 +79,7 @@ struct WorkIter {
     int64_t u, u_end, L;
     int32_t koff, dp, C, T, KB;
 
-    __device__ __forceinline__ void init(const GemmParams &p, int32_t cluster, int32_t nclusters)
+    __host__ __device__ __forceinline__ void init(const GemmParams &p, int32_t cluster, int32_t nclusters)
     {
         KB = p.num_k_blocks;
         C = nclusters;
@@ -98,7 +100,7 @@ struct WorkIter {
         }
     }
 
-    __device__ __forceinline__ bool next(WorkItem &w)
+    __host__ __device__ __forceinline__ bool next(WorkItem &w)
     {
         if (u < u_end) {
             const int64_t t = u / L;
@@ -128,7 +130,7 @@ struct ContribIter {
     int64_t lo, hi;
     int32_t j, n, tile;
 
-    __device__ __forceinline__ void init(const GemmParams &p, int32_t tile_, int32_t owner, int32_t C)
+    __host__ __device__ __forceinline__ void init(const GemmParams &p, int32_t tile_, int32_t owner, int32_t C)
     {
         tile = tile_;
         n = sk_ranges(p, C);
@@ -141,7 +143,7 @@ struct ContribIter {
         j = p.sk_head > 0 ? (int32_t)((int64_t)tile * n / p.sk_tiles) : owner + 1;
     }
 
-    __device__ __forceinline__ bool next(const GemmParams &p, int32_t &slot)
+    __host__ __device__ __forceinline__ bool next(const GemmParams &p, int32_t &slot)
     {
         for (; j < n; ++j) {
             const int64_t b = sk_begin(p, j, n);
