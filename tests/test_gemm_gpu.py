@@ -789,3 +789,41 @@ def test_gemm_convenience_matches_oracle():
     D = binding.gemm(A.cuda(), B.cuda())
     torch.cuda.synchronize()
     check(D.cpu(), A, B, 384, 640, 320)
+
+
+# ------------------------------------------------------------------ random shapes and options
+def _random_case(i: int):
+    rng = np.random.default_rng(1000 + i)
+    logu = lambda lo, hi: int(round(math.exp(rng.uniform(math.log(lo), math.log(hi)))))
+    if i % 2 == 0:  # edge-heavy: many tiny and thin shapes
+        M, N = logu(1, 3000), logu(1, 3000)
+    else:  # several tiles, where the k splits happen
+        M, N = int(rng.integers(200, 3001)), int(rng.integers(200, 3001))
+    K = 8 * logu(1, 2048)
+    opts = dict(cta_group=int(rng.integers(0, 3)), stream_k=int(rng.integers(0, 4)),
+                epi_schedule=int(rng.integers(0, 2)), scheduler=int(rng.integers(0, 2)),
+                k_order=int(rng.integers(0, 2)))
+    if rng.random() < 0.5:
+        opts["max_ctas"] = 2 * int(rng.integers(1, 21))
+    ldd = N + (int(rng.integers(1, 10)) if rng.random() < 0.3 else 0)
+    pad = 8 * int(rng.integers(1, 4)) if rng.random() < 0.3 else 0
+    return M, N, K, ldd, pad, opts
+
+
+@pytest.mark.parametrize("i", range(64))
+def test_random_shapes_and_options_exact(i):
+    # integer inputs keep every fp32 partial sum exact, so any split of k, any
+    # schedule and any tile order must give the oracle's bits
+    M, N, K, ldd, pad, opts = _random_case(i)
+    A, B = inputs.make_problem(M, N, K, "int2", seed=2000 + i, lda=K + pad, ldb=K + pad)
+    with binding.Gemm(0, **opts) as g:
+        info = g.plan(M, N, K, K + pad, K + pad, ldd)
+    if opts["stream_k"] == 0:
+        assert info["sk_tiles"] == 0 and info["sk_head"] == 0
+    if opts["stream_k"] == 2:
+        assert info["sk_head"] == 0
+    clusters = info["grid_ctas"] // info["cta_group"]
+    if info["sk_head"]:
+        assert info["sk_tiles"] == info["tiles"] < clusters and 0 < info["sk_head"] < info["k_blocks"]
+    D = run_gpu(A, B, M, N, K, ldd=ldd, **opts)
+    check(D, A, B, M, N, K, rows=sample_rows(M, extra=8, seed=i), exact=True)
