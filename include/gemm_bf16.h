@@ -98,7 +98,10 @@ typedef enum gemm_bf16_option {
                                         1 = TMA store (run fails with ALIGNMENT if not allowed);
                                         2 = masked coalesced st.global */
     GEMM_BF16_OPT_MAX_CTAS = 9,      /* upper bound on the persistent grid (0 = no bound) */
-    GEMM_BF16_OPT_WATCHDOG_NS = 10,  /* limit of every in-kernel barrier wait, ns (default 1e9) */
+    GEMM_BF16_OPT_WATCHDOG_NS = 10,  /* limit of every in-kernel barrier wait, ns (default 1e9).
+                                        plan raises it to 2 us per 64-wide k-block of K when that
+                                        is longer: no wait outlasts one tile's k-range of MMAs
+                                        (~0.3 us per k-block), so long-k problems never trip it */
     GEMM_BF16_OPT_FAULT_SKIP_LOAD = 11, /* test hook: each CTA's producer skips its load at this
                                           ring iteration, so the MMA warp's wait runs out and
                                           the kernel reports GEMM_BF16_ERR_DEVICE_TIMEOUT;

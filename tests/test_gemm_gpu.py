@@ -357,8 +357,10 @@ def test_stream_k_head_tail_exact(cta_group, M, N, K, max_ctas):
 
 
 @pytest.mark.parametrize("cta_group", [1, 2])
-@pytest.mark.parametrize("sched", SCHEDULES)
+@pytest.mark.parametrize("sched", SCHEDULES + [dict(acc_buffers=1), dict(acc_buffers=1, scheduler=1)])
 def test_schedules_with_head_tail_split(cta_group, sched):
+    # the owner folds the tails' partials into its spare accumulator only with
+    # the cooperative epilogue and two accumulators; otherwise after its MMAs
     M, N, K, max_ctas = 600, 700, 8200, 20
     A, B = inputs.make_problem(M, N, K, "int2", seed=41)
     with binding.Gemm(0, cta_group=cta_group, max_ctas=max_ctas, stream_k=3, **sched) as g:
@@ -765,6 +767,16 @@ def test_watchdog_reports_timeout_and_context_survives(variant):
     torch.cuda.synchronize()
     # the context is still usable: a normal run afterwards is correct
     check(run_gpu(A, B, M, N, K, **variant), A, B, M, N, K)
+
+
+@pytest.mark.parametrize("stream_k", [0, 1])
+def test_watchdog_limit_scales_with_k(stream_k):
+    # 1 us asked for, but a wait for a whole tile's accumulator (1024 k-blocks,
+    # ~0.3 ms) is legitimate: plan raises the limit to 2 us per k-block
+    M, N, K = 512, 512, 65536
+    A, B = inputs.make_problem(M, N, K, "int2", seed=81)
+    D = run_gpu(A, B, M, N, K, watchdog_ns=1000, stream_k=stream_k)
+    check(D, A, B, M, N, K, rows=sample_rows(M, extra=4), exact=True)
 
 
 def test_run_host_end_to_end():

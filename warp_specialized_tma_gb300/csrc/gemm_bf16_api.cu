@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kNumOptions = 20;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
+constexpr uint64_t kWatchdogNsPerKBlock = 2000;  // lower bound of the watchdog limit per k-block of K
 
 struct Plan {
     bool valid = false;
@@ -444,6 +445,11 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
     pl.num_m_blocks = (int)((M + (int64_t)kBlockM * cg - 1) / ((int64_t)kBlockM * cg));
     pl.num_n_blocks = (int)((N + kBlockN - 1) / kBlockN);
     pl.num_k_blocks = (int)((K + kBlockK - 1) / kBlockK);
+    // No in-kernel wait lasts longer than about one tile's k-range of MMAs (the
+    // epilogue waiting for an accumulator, an owner for a partial), ~0.3 us per
+    // k-block on GB300: a limit of 2 us per k-block keeps a long-k problem from
+    // tripping the watchdog, whatever the limit asked for.
+    pl.watchdog_ns = std::max<uint64_t>(pl.watchdog_ns, (uint64_t)pl.num_k_blocks * kWatchdogNsPerKBlock);
     pl.tiles = (int64_t)pl.num_m_blocks * pl.num_n_blocks;
     if (pl.tiles > kMaxDim / 2)
         return GEMM_BF16_ERR_INVALID_ARG;

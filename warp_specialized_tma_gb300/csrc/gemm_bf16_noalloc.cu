@@ -39,6 +39,7 @@ constexpr int kScratchWordsNeeded = 1;
 constexpr int kScratchWordsMax = 64;
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWatchdogNs = 1000000000ull;
+constexpr uint64_t kWatchdogNsPerKBlock = 2000;  // no wait outlasts one tile's k-range of MMAs
 
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kScratchWordsMax];
 
@@ -204,7 +205,9 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     prm.ldd = ldd;
     prm.D = D;
     prm.err = ds->scratch;  // word 0 of the shared scratch array
-    prm.watchdog_ns = kWatchdogNs;
+    prm.watchdog_ns = kWatchdogNs > (uint64_t)prm.num_k_blocks * kWatchdogNsPerKBlock
+                          ? kWatchdogNs
+                          : (uint64_t)prm.num_k_blocks * kWatchdogNsPerKBlock;
     prm.sk_tiles = 0;  // stream-K needs a partials workspace, which this entry point does not have
     prm.epoch = 1;
     prm.sk_units = 0;
