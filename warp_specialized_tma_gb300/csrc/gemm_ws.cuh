@@ -562,8 +562,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             }
             tile_parity ^= 1u;
         }
+        // The staging buffers must have been read before the CTA exits; the
+        // stores' writes to D complete before the grid is reported complete.
         if (lane == 0)
-            bulk_wait_all();
+            bulk_wait_read_all();
         __syncwarp();
     }
 
