@@ -159,11 +159,15 @@ typedef enum gemm_bf16_option {
                                         only the fp32 summation order (within the rounding bound;
                                         results stay deterministic).  Measured on 8192^3: DRAM reads
                                         -15%, and under the power cap +1% throughput */
-    GEMM_BF16_OPT_SERPENTINE = 19     /* tile order: 1 (default) = odd bands of RASTER_GROUP tile rows
+    GEMM_BF16_OPT_SERPENTINE = 19,    /* tile order: 1 (default) = odd bands of RASTER_GROUP tile rows
                                         walk their columns right to left, so a band's first tiles
                                         reuse the B panels the previous band read last (8192^3: DRAM
                                         reads -8.6%, +1% under the power cap); 0 = every band left
                                         to right */
+    GEMM_BF16_OPT_FAULT_TENSORMAP = 20 /* test hook: 1 = every run of the handle fails its tensor-map
+                                        encode as a driver error would, and returns
+                                        GEMM_BF16_ERR_TENSORMAP before launching anything;
+                                        0 (default) = off */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */

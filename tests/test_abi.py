@@ -108,3 +108,11 @@ def test_plan_info_struct_matches_the_header():
     assert [n for n, _ in got] == [n for _, n in fields]
     for (name, tname), (ctype, _) in zip(got, fields):
         assert tname in (ctypes_of[ctype], "c_" + ctype.replace("_t", "")), (name, tname, ctype)
+
+
+def test_option_keys_match_the_header():
+    # binding.OPTIONS mirrors gemm_bf16_option: same names (lower case) and values
+    text = open(HEADER).read()
+    body = re.search(r"typedef enum gemm_bf16_option \{(.*?)\} gemm_bf16_option;", text, re.S).group(1)
+    declared = {name.lower(): int(value) for name, value in re.findall(r"GEMM_BF16_OPT_(\w+)\s*=\s*(\d+)", body)}
+    assert declared == binding.OPTIONS

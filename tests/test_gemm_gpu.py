@@ -78,6 +78,31 @@ def check(D, A, B, M, N, K, rows=None, exact=False):
     return float(np.max(err)) if err.size else 0.0
 
 
+def _ordered(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> integers whose differences count ulps across zero."""
+    b = bits.astype(np.int64)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+
+
+def parity_stats(D, A, B, M, N, K, rows):
+    """Against the oracle on `rows`: errors vs the unrounded fp64 sum, the
+    tolerance count, and the exact-match fraction and ulp histogram vs the
+    oracle's bf16 rounding (a correct kernel differs from it only by rounding
+    flips and fp32 accumulation error, which matters most near zero)."""
+    ref64, refbf = oracle.gemm_rows(inputs.bits(A), inputs.bits(B), K=K, rows=rows)
+    got_bits = inputs.bits(D)[rows][:, :N]
+    got = inputs.from_bits(np.ascontiguousarray(got_bits)).double().numpy()
+    tol = 4e-3 * np.abs(ref64) + 2e-3 * math.sqrt(K) * rms(A, K) * rms(B, K)
+    err = np.abs(got - ref64)
+    ulp = np.abs(_ordered(got_bits) - _ordered(refbf))
+    big = np.abs(ref64) >= 0.25 * math.sqrt(K) * rms(A, K) * rms(B, K)  # a quarter of the typical size or more
+    return {"elements": int(err.size), "over_tolerance": int((~(err <= tol)).sum()),
+            "max_abs_err": float(err.max()), "max_err_over_tol": float((err / tol).max()),
+            "exact_frac": float((ulp == 0).mean()),
+            "ulp_hist": {str(k): int((ulp == k).sum()) for k in (0, 1, 2)} | {"3+": int((ulp >= 3).sum())},
+            "max_ulp_away_from_zero": int(ulp[big].max()) if big.any() else 0}
+
+
 def sample_rows(M: int, tile_m: int = 128, seed: int = 0, extra: int = 16):
     """First/last row of every 128-row slab plus random rows."""
     rng = np.random.default_rng(seed)
@@ -502,8 +527,14 @@ def test_workload_sampled_rows(name):
     M, N, K = w["M"], w["N"], w["K"]
     A, B = inputs.make_workload(name)
     D = run_gpu(A, B, M, N, K)
-    rows = sample_rows(M) if M > 512 else None
+    rows = sample_rows(M) if M > 512 else np.arange(M)
     check(D, A, B, M, N, K, rows=rows)
+    st = parity_stats(D, A, B, M, N, K, rows)
+    print(f"parity {name}: {st}")
+    assert st["over_tolerance"] == 0
+    # away from zero the fp32 sum is far closer than a bf16 ulp to the exact
+    # one, so the result is the oracle's rounding or its neighbour
+    assert st["max_ulp_away_from_zero"] <= 1
 
 
 @pytest.mark.parametrize("name", list(inputs.WORKLOADS))
@@ -777,6 +808,30 @@ def test_watchdog_limit_scales_with_k(stream_k):
     A, B = inputs.make_problem(M, N, K, "int2", seed=81)
     D = run_gpu(A, B, M, N, K, watchdog_ns=1000, stream_k=stream_k)
     check(D, A, B, M, N, K, rows=sample_rows(M, extra=4), exact=True)
+
+
+def test_tensormap_failure_is_reported_before_launch():
+    # an encode failure (forced by the test hook) comes back as TENSORMAP and
+    # launches nothing; the handle works again once the hook is off
+    M, N, K = 300, 260, 200
+    A, B = inputs.make_problem(M, N, K, "int2", seed=83, lda=pad8(K), ldb=pad8(K))
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.full((M, N), SENTINEL_BITS, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    with binding.Gemm(0, fault_tensormap=1) as g:
+        g.plan(M, N, K, pad8(K), pad8(K), N)
+        for _ in range(2):
+            with pytest.raises(binding.GemmError) as e:
+                g.run(dA, dB, dD)
+            assert e.value.status == binding.ERR_TENSORMAP
+        torch.cuda.synchronize()
+        assert bool((dD.view(torch.int16) == SENTINEL_BITS).all())
+        assert g.device_status()[0] == binding.OK
+        g.set_option("fault_tensormap", 0)
+        g.run(dA, dB, dD)
+        assert g.device_status()[0] == binding.OK
+    torch.cuda.synchronize()
+    check(dD.cpu(), A, B, M, N, K, exact=True)
 
 
 def test_run_host_end_to_end():

@@ -51,6 +51,7 @@ OPTIONS = {
     "repack": 17,
     "k_order": 18,
     "serpentine": 19,
+    "fault_tensormap": 20,
 }
 
 # the C entry points and their signatures

@@ -50,8 +50,8 @@ def source_digest() -> str:
 # What decides the GEMM kernel's behaviour on a given problem: its device code
 # and the host planner that picks its launch shape (not the public header's
 # documentation, the binding or the other kernels).
-KERNEL_FILES = ["gemm_ws.cuh", "gemm_common.cuh", "ptx.cuh", "gemm_kernels.h", "gemm_ws_c1.cu", "gemm_ws_c2.cu",
-                "gemm_bf16_api.cu"]
+KERNEL_FILES = ["gemm_ws.cuh", "gemm_common.cuh", "ptx.cuh", "ring_index.h", "gemm_kernels.h", "gemm_ws_c1.cu",
+                "gemm_ws_c2.cu", "gemm_bf16_api.cu"]
 
 
 def kernel_digest() -> str:

@@ -22,7 +22,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 20;
+constexpr int kNumOptions = 21;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 constexpr uint64_t kWatchdogNsPerKBlock = 2000;  // lower bound of the watchdog limit per k-block of K
 
@@ -113,6 +113,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_REPACK: return 0;
     case GEMM_BF16_OPT_K_ORDER: return 1;
     case GEMM_BF16_OPT_SERPENTINE: return 1;
+    case GEMM_BF16_OPT_FAULT_TENSORMAP: return 0;
     default: return 0;
     }
 }
@@ -139,6 +140,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_REPACK: return v >= 0 && v <= 2;
     case GEMM_BF16_OPT_K_ORDER: return v == 0 || v == 1;
     case GEMM_BF16_OPT_SERPENTINE: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_FAULT_TENSORMAP: return v == 0 || v == 1;
     default: return false;
     }
 }
@@ -710,7 +712,13 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     const int64_t lda_e = pack_a ? pl.ldp : pl.lda;
     const int64_t ldb_e = pack_b ? pl.ldp : pl.ldb;
 
-    if (!h->maps_valid || h->mA != Ae || h->mB != Be || h->mD != D) {
+    // test hook: the encode fails as a driver error would, before any launch
+    const bool fault_maps = h->opt[GEMM_BF16_OPT_FAULT_TENSORMAP] != 0;
+    if (fault_maps || !h->maps_valid || h->mA != Ae || h->mB != Be || h->mD != D) {
+        if (fault_maps) {
+            h->maps_valid = false;
+            return GEMM_BF16_ERR_TENSORMAP;
+        }
         const uint32_t b_rows = (uint32_t)(kBlockN / pl.cta_group);
         if ((rc = encode_2d(&h->tmA, Ae, (uint64_t)pl.K, (uint64_t)pl.M, (uint64_t)lda_e * 2, kBlockK, kBlockM)) ||
             (rc = encode_2d(&h->tmB, Be, (uint64_t)pl.K, (uint64_t)pl.N, (uint64_t)ldb_e * 2, kBlockK, b_rows))) {

@@ -6,6 +6,7 @@
 
 #include "gemm_kernels.h"
 #include "ptx.cuh"
+#include "ring_index.h"
 
 namespace wstma {
 

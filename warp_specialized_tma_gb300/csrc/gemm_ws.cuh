@@ -214,9 +214,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     // wait until the MMAs that read this stage (group) one lap ago
                     // have retired; a group of G stages is released by one commit
-                    if (((uint32_t)s & g_mask) == 0u &&
-                        !ctl.wait<kCluster>(empty_bar + 8u * ((uint32_t)s >> g_shift), ph ^ 1u, kRoleProducer,
-                                            (uint32_t)s)) {
+                    if (ring_group_first(s, g_mask) &&
+                        !ctl.wait<kCluster>(empty_bar + 8u * ring_group(s, g_shift), ring_empty_parity(ph),
+                                            kRoleProducer, (uint32_t)s)) {
                         ok = false;
                         break;
                     }
@@ -235,10 +235,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         }
                     }
                     ++it;
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    ring_advance(s, ph, S);
                 }
                 if (!ok)
                     break;
@@ -269,8 +266,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const int32_t j = it - d;
                     if (j == p.fault_skip_it)
                         continue;
-                    ctl.wait_drain<kCluster>(full_bar + 8u * (uint32_t)(j % S), (uint32_t)((j / S) & 1),
-                                             (uint32_t)(j % S));
+                    ctl.wait_drain<kCluster>(full_bar + 8u * (uint32_t)ring_stage_of(j, S), ring_parity_of(j, S),
+                                             (uint32_t)ring_stage_of(j, S));
                 }
             } else if (ctl.aborted()) {
                 // The peer's loads complete on the leader's barriers, which this CTA
@@ -313,7 +310,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBlockN);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!ready && !ctl.wait<kCluster>(full_bar + 8u * s, ph, kRoleMmaFull, (uint32_t)s)) {
+                    if (!ready && !ctl.wait<kCluster>(full_bar + 8u * s, ring_full_parity(ph), kRoleMmaFull, (uint32_t)s)) {
                         ok = false;
                         break;
                     }
@@ -327,20 +324,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     // the stage group is free once its MMAs have read it.  One commit
                     // per G k-blocks: measured on GB300, a commit every 4 MMAs keeps the
                     // tensor pipe ~93% busy, one every 8 MMAs keeps it ~100% busy.
-                    if (((uint32_t)s & g_mask) == g_mask) {
+                    if (ring_group_last(s, g_mask)) {
                         if constexpr (kCluster)
-                            mma_commit_pair(empty_bar + 8u * ((uint32_t)s >> g_shift), (uint16_t)0x3);
+                            mma_commit_pair(empty_bar + 8u * ring_group(s, g_shift), (uint16_t)0x3);
                         else
-                            mma_commit(empty_bar + 8u * ((uint32_t)s >> g_shift));
+                            mma_commit(empty_bar + 8u * ring_group(s, g_shift));
                     }
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    ring_advance(s, ph, S);
                     // Look at the next slot without blocking (try_wait with a zero
                     // suspend hint).  Measured on GB300: a test_wait probe here costs
                     // ~7% of the tensor pipe's throughput, a try_wait probe nothing.
-                    ready = mbar_try_wait<kCluster>(full_bar + 8u * s, ph, 0u);
+                    ready = mbar_try_wait<kCluster>(full_bar + 8u * s, ring_full_parity(ph), 0u);
                 }
                 if (!ok)
                     break;
