@@ -33,6 +33,14 @@
 //   tiles     static (default): every role walks the same grid-stride sequence;
 //             dynamic: the leader's producer takes whole tiles from a global
 //             counter and publishes them through the schedule ring.
+//
+// Split tiles (stream-K, GemmParams::sk_*): before its whole tiles, each SM
+// (pair) may take part of a tile's k-range.  Either the tiles of a partial last
+// wave are cut into equal shares, or, with fewer tiles than SM (pairs), every
+// tile is cut at one k-block into a head, computed by its owner, and a tail,
+// shared by the other SM (pairs).  A contributor leaves its fp32 partial in a
+// workspace slot and raises a flag; the owner adds the partials before its
+// epilogue stores the tile (gemm_common.cuh: WorkIter, ContribIter).
 #pragma once
 
 #include "gemm_common.cuh"
