@@ -289,15 +289,20 @@ __device__ __forceinline__ void epilogue_fused(uint32_t (&v0)[32], uint32_t (&v1
 // A CTA's fp32 partial accumulator (128 rows x 256 columns) in its workspace
 // slot, laid out as the epilogue holds it: for warp ew, chunk c, the 64 values
 // of each lane's row go as 16 float4 groups j, and group j of all 32 lanes is
-// 512 contiguous bytes (coalesced stores and loads).
+// 512 contiguous bytes (coalesced stores and loads).  A lane whose row or chunk
+// lies outside D (`live` false) neither stores nor reads its part: contributor
+// and owner skip the same parts, which matters for thin problems, where most
+// of a tile is padding.
 __device__ __forceinline__ float4 *partial_addr(float *slot, int ew, int c, int j, int lane)
 {
     return reinterpret_cast<float4 *>(slot) + (((ew * 2 + c) * 16 + j) * 32 + lane);
 }
 
-__device__ __forceinline__ void partial_store(float *slot, int ew, int c, int lane, const uint32_t (&v0)[32],
-                                              const uint32_t (&v1)[32])
+__device__ __forceinline__ void partial_store(float *slot, int ew, int c, int lane, bool live,
+                                              const uint32_t (&v0)[32], const uint32_t (&v1)[32])
 {
+    if (!live)
+        return;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const uint32_t *v = j < 8 ? &v0[4 * j] : &v1[4 * (j - 8)];
@@ -307,9 +312,15 @@ __device__ __forceinline__ void partial_store(float *slot, int ew, int c, int la
     }
 }
 
-__device__ __forceinline__ void partial_load(float *slot, int ew, int c, int lane, uint32_t (&v0)[32],
+__device__ __forceinline__ void partial_load(float *slot, int ew, int c, int lane, bool live, uint32_t (&v0)[32],
                                              uint32_t (&v1)[32])
 {
+    if (!live) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            v0[i] = v1[i] = 0u;
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const float4 f = __ldcg(partial_addr(slot, ew, c, j, lane));
@@ -321,9 +332,11 @@ __device__ __forceinline__ void partial_load(float *slot, int ew, int c, int lan
     }
 }
 
-__device__ __forceinline__ void partial_add(float *slot, int ew, int c, int lane, uint32_t (&v0)[32],
+__device__ __forceinline__ void partial_add(float *slot, int ew, int c, int lane, bool live, uint32_t (&v0)[32],
                                             uint32_t (&v1)[32])
 {
+    if (!live)
+        return;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const float4 f = __ldcg(partial_addr(slot, ew, c, j, lane));

@@ -406,6 +406,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const bool parked = p.sk_head > 0 && cluster_id < p.sk_tiles && !pingpong && p.acc_buffers == 2;
         if (parked) {
             const uint32_t spare = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kBlockN + col0);
+            const TileCoord htc = tile_coord(cluster_id, p);  // the head's tile
+            const bool row_live = htc.mb * kTileM + (int32_t)rank * kBlockM + q * 32 + lane < p.M;
             ContribIter ci;
             ci.init(p, cluster_id, cluster_id, num_clusters);
             int32_t s2;
@@ -420,16 +422,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const int pw = (col >> 7) * 4 + q;
                     const int pc = (col >> 6) & 1;
                     float *const part = p.workspace + (size_t)slot2 * kPartialFloats;
+                    const bool live = row_live && htc.nb * kBlockN + col < p.N;
                     uint32_t v0[32], v1[32];
                     if (first) {
-                        partial_load(part, pw, pc, lane, v0, v1);
+                        partial_load(part, pw, pc, lane, live, v0, v1);
                     } else {
                         tmem_load_32x32(spare + (uint32_t)(c * 64), v0);
                         tmem_load_32x32(spare + (uint32_t)(c * 64 + 32), v1);
                         tmem_load_wait();
                         reg_fence(v0);
                         reg_fence(v1);
-                        partial_add(part, pw, pc, lane, v0, v1);
+                        partial_add(part, pw, pc, lane, live, v0, v1);
                     }
                     tmem_store_32x32(spare + (uint32_t)(c * 64), v0);
                     tmem_store_32x32(spare + (uint32_t)(c * 64 + 32), v1);
@@ -526,8 +529,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                             mbar_arrive(acce_bar + 8u * acc);
                     }
                 }
+                const int32_t x = tc.nb * kBlockN + col;
+                // parts of a split tile outside D are neither stored nor read
+                const bool live = y + lane < p.M && x < p.N;
                 if (contributor) {
-                    partial_store(p.workspace + (size_t)slot_id * kPartialFloats, pw, pc, lane, v0, v1);
+                    partial_store(p.workspace + (size_t)slot_id * kPartialFloats, pw, pc, lane, live, v0, v1);
                     continue;
                 }
                 if (owner && !parked) {
@@ -538,10 +544,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         const int32_t slot2 = s2 * CG + (int32_t)rank;
                         if (c == 0 && !warp_wait_flag(ctl, p.flags + slot2, p.epoch, lane))
                             break;
-                        partial_add(p.workspace + (size_t)slot2 * kPartialFloats, pw, pc, lane, v0, v1);
+                        partial_add(p.workspace + (size_t)slot2 * kPartialFloats, pw, pc, lane, live, v0, v1);
                     }
                 }
-                const int32_t x = tc.nb * kBlockN + col;
                 if (p.fused)
                     epilogue_fused(v0, v1, x, y + lane, p);
                 epilogue_store_chunk(v0, v1, staging, lane, tma_store, &tmD, x, y, p);
