@@ -894,3 +894,25 @@ def test_random_shapes_and_options_exact(i):
         assert info["sk_tiles"] == info["tiles"] < clusters and 0 < info["sk_head"] < info["k_blocks"]
     D = run_gpu(A, B, M, N, K, ldd=ldd, **opts)
     check(D, A, B, M, N, K, rows=sample_rows(M, extra=8, seed=i), exact=True)
+
+
+def test_binding_rejects_tensors_off_the_handles_device():
+    # the library dereferences raw pointers on the handle's device only; the
+    # binding refuses host tensors for run() and device tensors as run_host's
+    # host side before anything reaches the library
+    M, N, K = 64, 64, 64
+    A, B = inputs.make_problem(M, N, K, "int2", seed=87)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0) as g:
+        assert g.device == 0
+        g.plan(M, N, K)
+        with pytest.raises(ValueError):
+            g.run(A, dB, dD)
+        with pytest.raises(ValueError):
+            g.run_host(dA, B, torch.empty((M, N), dtype=torch.bfloat16), dA, dB, dD)
+        g.run(dA, dB, dD)
+        assert g.device_status()[0] == binding.OK
+    torch.cuda.synchronize()
+    check(dD.cpu(), A, B, M, N, K, exact=True)

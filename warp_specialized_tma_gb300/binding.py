@@ -221,10 +221,10 @@ def _check(st: int, what: str) -> None:
         raise GemmError(st, what)
 
 
-def _stream_handle(stream) -> int:
+def _stream_handle(stream, device=None) -> int:
     import torch
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -241,9 +241,13 @@ class Gemm:
     """
 
     def __init__(self, device: int = -1, **options):
+        import torch
         st, h = gemm_bf16_create(device)
         _check(st, "gemm_bf16_create")
         self.h = h
+        # the device the handle is bound to: the library dereferences the raw
+        # pointers it is given on this device only
+        self.device = int(device) if device >= 0 else torch.cuda.current_device()
         self.shape = None
         for k, v in options.items():
             self.set_option(k, v)
@@ -269,6 +273,11 @@ class Gemm:
         _check(st, "gemm_bf16_plan_info")
         return info.as_dict()
 
+    def _on_device(self, *tensors) -> None:
+        for t in tensors:
+            if t.device.type != "cuda" or t.device.index != self.device:
+                raise ValueError(f"tensors must be on cuda:{self.device}, the handle's device (got {t.device})")
+
     def _validate(self, A, B, D) -> None:
         import torch
         if self.shape is None:
@@ -288,7 +297,8 @@ class Gemm:
         self._validate(A, B, D)
         if not (A.is_cuda and B.is_cuda and D.is_cuda):
             raise ValueError("run() takes device tensors; use run_host() for host operands")
-        _check(gemm_bf16_run(self.h, A.data_ptr(), B.data_ptr(), D.data_ptr(), _stream_handle(stream)),
+        self._on_device(A, B, D)
+        _check(gemm_bf16_run(self.h, A.data_ptr(), B.data_ptr(), D.data_ptr(), _stream_handle(stream, self.device)),
                "gemm_bf16_run")
 
     def run_fused(self, A, B, D, C=None, bias=None, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
@@ -303,17 +313,22 @@ class Gemm:
             ldc = _ld(C, M, "C")
         if bias is not None and (bias.dtype != torch.bfloat16 or not bias.is_cuda or bias.numel() < N):
             raise TypeError("bias must be a bf16 device tensor with N values")
+        self._on_device(A, B, D, *(t for t in (C, bias) if t is not None))
         _check(gemm_bf16_run_fused(self.h, A.data_ptr(), B.data_ptr(), D.data_ptr(),
                                    0 if C is None else C.data_ptr(), ldc,
                                    0 if bias is None else bias.data_ptr(), alpha, beta,
-                                   _stream_handle(stream)), "gemm_bf16_run_fused")
+                                   _stream_handle(stream, self.device)), "gemm_bf16_run_fused")
 
     def run_host(self, hA, hB, hD, dA, dB, dD, stream=None) -> None:
         """Copies hA, hB to dA, dB, runs, copies the result to hD (all enqueued on `stream`)."""
         self._validate(hA, hB, hD)
         self._validate(dA, dB, dD)
+        if hA.is_cuda or hB.is_cuda or hD.is_cuda:
+            raise ValueError("run_host() takes host tensors hA, hB, hD")
+        self._on_device(dA, dB, dD)
         _check(gemm_bf16_run_host(self.h, hA.data_ptr(), hB.data_ptr(), hD.data_ptr(), dA.data_ptr(),
-                                  dB.data_ptr(), dD.data_ptr(), _stream_handle(stream)), "gemm_bf16_run_host")
+                                  dB.data_ptr(), dD.data_ptr(), _stream_handle(stream, self.device)),
+               "gemm_bf16_run_host")
 
     def device_status(self):
         """(status, detail word) of the device watchdog; synchronises the last stream."""
