@@ -284,10 +284,10 @@ GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail);
 
 /* GEMM for callers that cannot allocate device memory (no counterpart in the
  * pages: this is a property of the library's interface, not of the method).
- * Code being captured into a CUDA graph, runtimes whose pool owns all device
- * memory, and loops that cannot afford an allocation's synchronisation cannot
- * call gemm_bf16_create (it allocates); they call this instead.  It keeps no
- * handle: it computes D = A * B^T exactly like gemm_bf16_run with the default
+ * Runtimes whose pool owns all device memory, and loops that cannot afford an
+ * allocation's synchronisation, cannot call gemm_bf16_create (it allocates);
+ * they call this instead.  It keeps no handle: it computes D = A * B^T
+ * exactly like gemm_bf16_run with the default
  * options (same arguments and alignment rules, same kernel), with A, B, D and
  * the stream supplied by the caller, and allocates nothing -- no cudaMalloc,
  * cudaFree or allocating library call.  Two parts of the default plan need

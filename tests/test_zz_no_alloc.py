@@ -1,5 +1,5 @@
 """The allocation-free entry point, for callers that cannot allocate device
-memory (graph capture, pool-owned memory, allocation-free loops).
+memory (pool-owned memory, loops that cannot afford an allocation).
 
 gemm_bf16_run_noalloc must give the same D as gemm_bf16_run on the same
 operands, within the tolerance the other GPU tests use, on two calls in a row

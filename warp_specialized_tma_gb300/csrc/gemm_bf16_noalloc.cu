@@ -1,7 +1,6 @@
 // gemm_bf16_run_noalloc: the GEMM for callers that must not allocate.
 //
 // Some callers cannot call cudaMalloc at the point where they multiply:
-// code recorded into a CUDA graph (allocation is not a capturable operation),
 // runtimes that own every byte of device memory through their own pool and
 // forbid raw allocations, and latency-critical loops where an allocation's
 // implicit synchronisation is not acceptable.  gemm_bf16_create() allocates (a
