@@ -6,7 +6,9 @@
 Prints the resolved plan, the mean CUDA-event time per launch, the TFLOP/s and
 the fraction of the roofline (the larger of the FLOPs at 2.25 PFLOP/s and the
 compulsory bytes at 8 TB/s).  This is the command the ncu summaries under
-profiles/ were taken with.
+profiles/ were taken with.  With --cublas, torch.matmul (cuBLAS) on the same
+operands is timed after the library, the same number of launches, as a
+comparator; it is not part of the library.
 """
 from __future__ import annotations
 
@@ -35,6 +37,8 @@ def main(argv=None) -> int:
     ap.add_argument("--device", type=int, default=0)
     ap.add_argument("--graph", action="store_true",
                     help="time the launches replayed from one CUDA graph (no host launch cost per launch)")
+    ap.add_argument("--cublas", action="store_true",
+                    help="also time torch.matmul(A, B.T) (cuBLAS) on the same operands, after the library's launches")
     args = ap.parse_args(argv)
 
     w = dict(inputs.WORKLOADS[args.workload])
@@ -77,6 +81,18 @@ def main(argv=None) -> int:
         torch.cuda.synchronize(dev)
         st, detail = g.device_status()
     ms = e0.elapsed_time(e1) / max(args.iters, 1)
+    cublas_ms = None
+    if args.cublas:
+        dD2 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(args.warmup):
+            torch.matmul(dA, dB.t(), out=dD2)
+        torch.cuda.synchronize(dev)
+        e0.record()
+        for _ in range(args.iters):
+            torch.matmul(dA, dB.t(), out=dD2)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        cublas_ms = e0.elapsed_time(e1) / max(args.iters, 1)
     flops = 2.0 * M * N * K
     nbytes = 2.0 * (M * K + N * K + M * N)  # compulsory: read A and B, write D once
     # roofline time: the larger of the FLOPs at the dense-bf16 tensor peak and
@@ -87,6 +103,9 @@ def main(argv=None) -> int:
            "roofline_us_nominal": roof_us,
            "roofline_bound": "tensor" if flops / NOMINAL_TFLOPS / 1e12 >= nbytes / NOMINAL_HBM_GBS / 1e9 else "hbm",
            "frac_of_roofline_nominal": roof_us / (ms * 1e3), "status": st, "detail": detail}
+    if cublas_ms is not None:
+        out["cublas_ms_per_launch"] = cublas_ms
+        out["cublas_tflops"] = flops / (cublas_ms * 1e-3) / 1e12
     print(json.dumps(out))
     return 0 if st == binding.OK else 1
 
