@@ -164,10 +164,29 @@ typedef enum gemm_bf16_option {
                                         reuse the B panels the previous band read last (8192^3: DRAM
                                         reads -8.6%, +1% under the power cap); 0 = every band left
                                         to right */
-    GEMM_BF16_OPT_FAULT_TENSORMAP = 20 /* test hook: 1 = every run of the handle fails its tensor-map
+    GEMM_BF16_OPT_FAULT_TENSORMAP = 20, /* test hook: 1 = every run of the handle fails its tensor-map
                                         encode as a driver error would, and returns
                                         GEMM_BF16_ERR_TENSORMAP before launching anything;
                                         0 (default) = off */
+    GEMM_BF16_OPT_THIN = 21           /* Problems with min(M, N) <= 64 (decode-like, bound by
+                                        streaming the other operand from HBM) can run on the thin
+                                        kernel: the large operand in 128-row tiles is the MMA's M
+                                        side, the small one its N side (rounded up to 16, 32, 48 or
+                                        64), one CTA per SM with a ring of up to 12 stages, the
+                                        (tile, k-block) units split evenly over the SMs, and split
+                                        tiles summed in a fixed order from fp32 partials in a
+                                        handle-owned workspace (2 slots of 128 x 64 fp32 per SM,
+                                        plus one counter per tile).  Of the other options only
+                                        WATCHDOG_NS, FAULT_SKIP_LOAD, PDL, REPACK and
+                                        FAULT_TENSORMAP apply to it.
+                                        1 (default) = automatic: the thin kernel where it measured
+                                        faster on GB300, min(M, N) <= 32 with max(M, N) >= 4096 and
+                                        K >= 1024, and only while every option that shapes the
+                                        square kernel (PIPELINE, CTA_GROUP, PERSISTENT, ACC_BUFFERS,
+                                        SETMAXNREG, STAGES, EPILOGUE, MAX_CTAS, STAGE_GROUP,
+                                        EPI_SCHEDULE, SCHEDULER) is at its default;
+                                        2 = the thin kernel whenever min(M, N) <= 64;
+                                        0 = never */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */
@@ -200,6 +219,9 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t serpentine;           /* 1 = odd tile bands walk right to left */
     int32_t sk_head;              /* > 0: every tile split at this k-block (head/tail stream-K) */
     int32_t sk_slots;             /* fp32 partial slots (128 x 256 each) the workspace holds */
+    int32_t thin;                 /* the thin kernel's small-operand width (16, 32, 48 or 64); 0 = the
+                                     square kernel.  Then tile_m = 128 rows of the large operand,
+                                     tile_n = thin, and tiles counts the large operand's tiles */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's

@@ -38,3 +38,20 @@ def test_work_split_and_tile_order(tmp_path):
     assert build.returncode == 0, build.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
     assert run.returncode == 0 and run.stdout.startswith("ok"), run.stdout + run.stderr
+
+
+def test_thin_kernel_work_split(tmp_path):
+    """The thin kernel's split (csrc/thin_split.h, plain C++): ranges, pieces,
+    partial slots and the epoch-tagged tile counter, checked by
+    tests/thin_split_check.cpp.  Needs a C++ compiler, not a GPU."""
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    exe = tmp_path / "thin_split_check"
+    build = subprocess.run(
+        [cxx, "-std=c++17", "-O2", "-I", os.path.join(ROOT, "warp_specialized_tma_gb300", "csrc"),
+         os.path.join(ROOT, "tests", "thin_split_check.cpp"), "-o", str(exe)],
+        capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
+    assert run.returncode == 0 and run.stdout.startswith("ok"), run.stdout + run.stderr

@@ -1,0 +1,169 @@
+"""GPU parity of the thin kernel (min(M, N) <= 64) against the CPU oracle.
+
+The thin kernel puts the large operand on the MMA's 128-row side and the small
+one, rounded up to 16, 32, 48 or 64 rows, on its N side; split tiles are
+summed from fp32 partials in a fixed order.  Integer-valued inputs make every
+sum exact, so there the result must equal the oracle's bf16 rounding bit for
+bit, in both orientations (small B: D rows are accumulator rows; small A: D
+is the accumulator transposed), with padded pitches, the fused epilogue,
+repeated launches of one handle and a watchdog give-up in between.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from warp_specialized_tma_gb300 import binding, inputs
+
+from test_gemm_gpu import SENTINEL_BITS, check, rms, run_fused_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from warp_specialized_tma_gb300 import build as libbuild
+    libbuild.build()
+    binding.load()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def nt_of(M, N):
+    small = N if N <= 64 else M
+    return (small + 15) // 16 * 16
+
+
+def run_thin(A, B, M, N, K, ldd=None, **opts):
+    """D on the GPU with the thin kernel forced; returns (D on the CPU, plan info)."""
+    ldd = N if ldd is None else ldd
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.full((M, ldd), SENTINEL_BITS, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    opts = {"thin": 2} | opts
+    with binding.Gemm(0, **opts) as g:
+        info = g.plan(M, N, K, A.shape[1], B.shape[1], ldd)
+        g.run(dA, dB, dD)
+        st, detail = g.device_status()
+        assert st == binding.OK, f"device status {st} detail {detail:#x}"
+    torch.cuda.synchronize()
+    return dD.cpu(), info
+
+
+SHAPES = [
+    # small B (D rows are accumulator rows)
+    (4096, 16, 4104), (1000, 1, 130), (300, 17, 64), (2048, 48, 1000), (129, 64, 8), (8192, 40, 2048),
+    # small A (D is the accumulator transposed)
+    (16, 4096, 4104), (1, 1000, 130), (17, 300, 64), (48, 2048, 1000), (64, 129, 8), (40, 8192, 2048),
+    # both small
+    (16, 16, 512), (7, 5, 3), (64, 64, 64),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_thin_exact_integers(shape):
+    M, N, K = shape
+    ld = (K + 7) // 8 * 8  # rows 16-byte aligned, as TMA needs
+    A, B = inputs.make_problem(M, N, K, "int2", seed=M * 7 + N * 3 + K, lda=ld, ldb=ld)
+    D, info = run_thin(A, B, M, N, K)
+    assert info["thin"] == nt_of(M, N) and info["cta_group"] == 1 and info["tile_m"] == 128
+    check(D, A, B, M, N, K, exact=True)
+
+
+@pytest.mark.parametrize("shape,pads", [((2048, 16, 1000), (1008, 1024, 24)), ((16, 2048, 1000), (1016, 1000, 2056)),
+                                        ((777, 33, 520), (520, 528, 40)), ((33, 777, 520), (528, 520, 780))],
+                         ids=["smallB", "smallA", "smallB33", "smallA33"])
+def test_thin_random_values_padded(shape, pads):
+    M, N, K = shape
+    lda, ldb, ldd = pads
+    A, B = inputs.make_problem(M, N, K, "normal", seed=91, lda=lda, ldb=ldb)
+    D, info = run_thin(A, B, M, N, K, ldd=ldd)
+    assert info["thin"] == nt_of(M, N)
+    check(D, A, B, M, N, K)  # also checks the padding columns of D keep the sentinel
+
+
+@pytest.mark.parametrize("shape", [(2048, 16, 1000), (16, 2048, 1000), (300, 40, 200), (40, 300, 200)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_thin_fused_exact_integers(shape):
+    M, N, K = shape
+    A, B = inputs.make_problem(M, N, K, "int2", seed=81)
+    g = torch.Generator().manual_seed(82)
+    C = inputs.make_operand(M, N, None, "int2", g)
+    bias = inputs.make_operand(1, N, None, "int2", g).reshape(-1)
+    D = run_fused_gpu(A, B, M, N, K, C=C, bias=bias, alpha=2.0, beta=-3.0, thin=2)
+    _, refbf = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 2.0, -3.0, C=inputs.bits(C),
+                                      bias=inputs.bits(bias))
+    assert np.array_equal(inputs.bits(D), refbf)
+
+
+def test_thin_fused_in_place_random_values():
+    M, N, K = 24, 1500, 704
+    A, B = inputs.make_problem(M, N, K, "normal", seed=83)
+    g = torch.Generator().manual_seed(84)
+    C = inputs.make_operand(M, N, None, "normal", g)
+    bias = inputs.make_operand(1, N, None, "uniform", g).reshape(-1)
+    D = run_fused_gpu(A, B, M, N, K, C=C, bias=bias, alpha=0.625, beta=1.25, inplace=True, thin=2)
+    ref64, _ = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 0.625, 1.25, C=inputs.bits(C),
+                                      bias=inputs.bits(bias))
+    tol = 4e-3 * np.abs(ref64) + 2e-3 * math.sqrt(K) * rms(A, K) * rms(B, K) * 0.625 + 1e-6
+    assert np.all(np.abs(D.double().numpy() - ref64) <= tol)
+
+
+def test_thin_repeated_launches_with_split_tiles():
+    # 64 tiles of 128 k-blocks over the SMs: tiles are split, so every launch
+    # counts pieces with a new epoch and the last piece sums the partials
+    M, N, K = 16, 8192, 8192
+    dev = torch.device("cuda:0")
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0, thin=2) as g:
+        info = g.plan(M, N, K)
+        assert info["thin"] == 16 and info["tiles"] == 64 and info["grid_ctas"] > info["tiles"]
+        for seed in (101, 102, 103):
+            A, B = inputs.make_problem(M, N, K, "int2", seed=seed)
+            g.run(A.to(dev), B.to(dev), dD)
+            assert g.device_status()[0] == binding.OK
+            check(dD.cpu(), A, B, M, N, K, exact=True)
+
+
+def test_thin_watchdog_gives_up_and_the_handle_recovers():
+    M, N, K = 16, 4096, 4096
+    A, B = inputs.make_problem(M, N, K, "int2", seed=111)
+    dev = torch.device("cuda:0")
+    dA, dB = A.to(dev), B.to(dev)
+    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0, thin=2, watchdog_ns=20_000_000, fault_skip_load=3) as g:
+        g.plan(M, N, K)
+        g.run(dA, dB, dD)
+        st, detail = g.device_status()
+        assert st == binding.ERR_DEVICE_TIMEOUT and detail != 0
+        g.set_option("fault_skip_load", -1)
+        g.plan(M, N, K)
+        g.run(dA, dB, dD)
+        assert g.device_status()[0] == binding.OK
+    check(dD.cpu(), A, B, M, N, K, exact=True)
+
+
+def test_thin_selection():
+    with binding.Gemm(0) as g:  # automatic (the default)
+        assert g.plan(16, 8192, 8192)["thin"] == 16
+        assert g.plan(1, 8192, 8192)["thin"] == 16
+        assert g.plan(8192, 32, 1024)["thin"] == 32
+        assert g.plan(8192, 33, 8192)["thin"] == 0  # 48 or 64 rows: the square kernel measured faster
+        assert g.plan(16, 4000, 8192)["thin"] == 0  # too little to stream
+        assert g.plan(16, 8192, 1016)["thin"] == 0
+        assert g.plan(8192, 8192, 8192)["thin"] == 0
+    with binding.Gemm(0, thin=2) as g:
+        assert g.plan(33, 33, 104)["thin"] == 48
+        assert g.plan(8192, 64, 8192)["thin"] == 64
+        assert g.plan(8192, 65, 8192)["thin"] == 0
+    with binding.Gemm(0, cta_group=1) as g:  # a square-kernel option: no automatic thin
+        assert g.plan(16, 8192, 8192)["thin"] == 0
+    with binding.Gemm(0, thin=2, cta_group=1) as g:
+        assert g.plan(16, 8192, 8192)["thin"] == 16
+    with binding.Gemm(0, thin=0) as g:
+        assert g.plan(16, 8192, 8192)["thin"] == 0

@@ -52,6 +52,7 @@ OPTIONS = {
     "k_order": 18,
     "serpentine": 19,
     "fault_tensormap": 20,
+    "thin": 21,
 }
 
 # the C entry points and their signatures
@@ -107,6 +108,7 @@ class PlanInfo(ctypes.Structure):
         ("serpentine", ctypes.c_int32),
         ("sk_head", ctypes.c_int32),
         ("sk_slots", ctypes.c_int32),
+        ("thin", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libgemm_bf16.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 SOURCES = ["gemm_bf16_api.cu", "gemm_ws_c1.cu", "gemm_ws_c2.cu", "gemm_nows.cu", "gemm_bf16_noalloc.cu",
-           "gemm_repack.cu"]
+           "gemm_repack.cu", "gemm_thin.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]

@@ -17,12 +17,13 @@
 #include <vector>
 
 #include "gemm_kernels.h"
+#include "thin_split.h"
 
 using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 21;
+constexpr int kNumOptions = 22;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 constexpr uint64_t kWatchdogNsPerKBlock = 2000;  // lower bound of the watchdog limit per k-block of K
 
@@ -49,6 +50,9 @@ struct Plan {
     int serpentine = 0;
     bool repack_a = false, repack_b = false;  // operands copied to a 128-byte-multiple pitch first
     int64_t ldp = 0;                          // that pitch in elements
+    int thin_nt = 0;                          // > 0: the thin kernel, small-operand width 16..64
+    bool thin_transposed = false;             // thin kernel: the large operand is B
+    int64_t thin_units = 0;                   // thin kernel: tiles * k-blocks
     int64_t tiles = 0;
     int num_m_blocks = 0, num_n_blocks = 0, num_k_blocks = 0;
     int grid_ctas = 0;
@@ -87,6 +91,11 @@ struct gemm_bf16 {
     // packed operand copies (A then B), grown on demand by plan
     void *pack = nullptr;
     size_t pack_bytes = 0;
+    // thin kernel's partials and per-tile counters, grown on demand by plan
+    float *thin_ws = nullptr;
+    size_t thin_ws_floats = 0;
+    uint32_t *thin_cnt = nullptr;
+    size_t thin_cnt_n = 0;
 };
 
 namespace {
@@ -114,6 +123,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_K_ORDER: return 1;
     case GEMM_BF16_OPT_SERPENTINE: return 1;
     case GEMM_BF16_OPT_FAULT_TENSORMAP: return 0;
+    case GEMM_BF16_OPT_THIN: return 1;
     default: return 0;
     }
 }
@@ -141,6 +151,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_K_ORDER: return v == 0 || v == 1;
     case GEMM_BF16_OPT_SERPENTINE: return v == 0 || v == 1;
     case GEMM_BF16_OPT_FAULT_TENSORMAP: return v == 0 || v == 1;
+    case GEMM_BF16_OPT_THIN: return v >= 0 && v <= 2;
     default: return false;
     }
 }
@@ -280,151 +291,12 @@ int prepare_kernel(const void *fn, size_t max_smem, int *regs)
     return GEMM_BF16_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-GEMM_BF16_API const char *gemm_bf16_strerror(int status)
+// The square kernel's plan: CTA mode, ring depth, kernel variant, persistent
+// grid and stream-K split (with its workspace).
+int plan_square(gemm_bf16_t h, Plan &pl)
 {
-    switch (status) {
-    case GEMM_BF16_OK: return "ok";
-    case GEMM_BF16_ERR_INVALID_ARG: return "invalid argument";
-    case GEMM_BF16_ERR_ALIGNMENT: return "alignment: TMA needs 16-byte aligned bases and row strides";
-    case GEMM_BF16_ERR_NOT_PLANNED: return "not planned: call gemm_bf16_plan first";
-    case GEMM_BF16_ERR_CUDA: return "a CUDA runtime call failed";
-    case GEMM_BF16_ERR_TENSORMAP: return "TMA tensor-map encoding failed";
-    case GEMM_BF16_ERR_DEVICE_TIMEOUT: return "device watchdog: a barrier wait ran out and the kernel returned early";
-    case GEMM_BF16_ERR_UNSUPPORTED: return "unsupported device or option combination";
-    default: return "unknown status";
-    }
-}
-
-GEMM_BF16_API const char *gemm_bf16_version(void) { return "gemm_bf16 1.0 sm_103a"; }
-
-GEMM_BF16_API int gemm_bf16_check_problem(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd)
-{
-    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-        return GEMM_BF16_ERR_INVALID_ARG;
-    if (lda < K || ldb < K || ldd < N)
-        return GEMM_BF16_ERR_INVALID_ARG;
-    if (lda > (int64_t(1) << 38) || ldb > (int64_t(1) << 38) || ldd > (int64_t(1) << 38))
-        return GEMM_BF16_ERR_INVALID_ARG;
-    if ((lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0)
-        return GEMM_BF16_ERR_ALIGNMENT;
-    return GEMM_BF16_OK;
-}
-
-GEMM_BF16_API int gemm_bf16_create(int device, gemm_bf16_t *out)
-{
-    if (!out)
-        return GEMM_BF16_ERR_INVALID_ARG;
-    *out = nullptr;
-    int dev = device;
-    if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_BF16_ERR_CUDA;
-    }
-    int count = 0;
-    if (cudaGetDeviceCount(&count) != cudaSuccess || dev >= count) {
-        cudaGetLastError();
-        return GEMM_BF16_ERR_CUDA;
-    }
-    if (cudaSetDevice(dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_BF16_ERR_CUDA;
-    }
-    int major = 0, minor = 0, sms = 0, optin = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_BF16_ERR_CUDA;
-    }
-    if (major != 10 || minor != 3)
-        return GEMM_BF16_ERR_UNSUPPORTED;
-    gemm_bf16_t h = new (std::nothrow) gemm_bf16();
-    if (!h)
-        return GEMM_BF16_ERR_CUDA;
-    h->device = dev;
-    h->num_sms = sms;
-    h->max_smem_optin = (size_t)optin;
-    for (int k = 0; k < kNumOptions; ++k)
-        h->opt[k] = default_option(k);
-    if (cudaMalloc(&h->d_err, 4 * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(h->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) {
-        cudaGetLastError();
-        if (h->d_err)
-            cudaFree(h->d_err);
-        delete h;
-        return GEMM_BF16_ERR_CUDA;
-    }
-    *out = h;
-    return GEMM_BF16_OK;
-}
-
-GEMM_BF16_API int gemm_bf16_destroy(gemm_bf16_t h)
-{
-    if (!h)
-        return GEMM_BF16_OK;
-    cudaSetDevice(h->device);
-    if (h->d_err)
-        cudaFree(h->d_err);
-    if (h->ws)
-        cudaFree(h->ws);
-    if (h->ws_flags)
-        cudaFree(h->ws_flags);
-    if (h->pack)
-        cudaFree(h->pack);
-    delete h;
-    return GEMM_BF16_OK;
-}
-
-GEMM_BF16_API int gemm_bf16_set_option(gemm_bf16_t h, int key, int64_t value)
-{
-    if (!h || key < 1 || key >= kNumOptions || !option_in_range(key, value))
-        return GEMM_BF16_ERR_INVALID_ARG;
-    h->opt[key] = value;
-    return GEMM_BF16_OK;
-}
-
-GEMM_BF16_API int gemm_bf16_get_option(gemm_bf16_t h, int key, int64_t *value)
-{
-    if (!h || !value || key < 1 || key >= kNumOptions)
-        return GEMM_BF16_ERR_INVALID_ARG;
-    *value = h->opt[key];
-    return GEMM_BF16_OK;
-}
-
-GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                                 int64_t ldd)
-{
-    if (!h)
-        return GEMM_BF16_ERR_INVALID_ARG;
-    h->plan.valid = false;
-    h->maps_valid = false;
-    int rc = gemm_bf16_check_problem(M, N, K, lda, ldb, ldd);
-    if (rc != GEMM_BF16_OK)
-        return rc;
-    if ((rc = set_device(h)) != GEMM_BF16_OK)
-        return rc;
-
-    Plan pl;
-    pl.M = M, pl.N = N, pl.K = K, pl.lda = lda, pl.ldb = ldb, pl.ldd = ldd;
-    pl.pipeline = (int)h->opt[GEMM_BF16_OPT_PIPELINE];
-    pl.persistent = (int)h->opt[GEMM_BF16_OPT_PERSISTENT];
-    pl.acc_buffers = (int)h->opt[GEMM_BF16_OPT_ACC_BUFFERS];
-    pl.setmaxnreg = (int)h->opt[GEMM_BF16_OPT_SETMAXNREG];
-    pl.raster_group = (int)h->opt[GEMM_BF16_OPT_RASTER_GROUP];
-    pl.epilogue_opt = (int)h->opt[GEMM_BF16_OPT_EPILOGUE];
-    pl.epi_pingpong = (int)h->opt[GEMM_BF16_OPT_EPI_SCHEDULE];
-    pl.sched_dynamic = (int)h->opt[GEMM_BF16_OPT_SCHEDULER];
-    pl.k_order = (int)h->opt[GEMM_BF16_OPT_K_ORDER];
-    pl.serpentine = (int)h->opt[GEMM_BF16_OPT_SERPENTINE];
-    pl.fault_skip = (int)h->opt[GEMM_BF16_OPT_FAULT_SKIP_LOAD];
-    pl.watchdog_ns = (uint64_t)h->opt[GEMM_BF16_OPT_WATCHDOG_NS];
-    pl.epi_tma_allowed = ((ldd * 2) % 16) == 0;
-
+    const int64_t M = pl.M, N = pl.N, K = pl.K;
+    int rc;
     int cg = (int)h->opt[GEMM_BF16_OPT_CTA_GROUP];
     const bool ws = pl.pipeline == GEMM_BF16_PIPE_WS;
     if (!ws) {
@@ -592,6 +464,254 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         h->ws_flags = nflags;
         h->ws_slots = pl.sk_slots;
     }
+    return GEMM_BF16_OK;
+}
+
+// The thin kernel's plan (gemm_thin.cuh): the large operand in 128-row tiles,
+// the small one as the MMA's N side, one CTA per SM, the (tile, k-block) units
+// split evenly, and the workspace for the split tiles' partials.
+int plan_thin(gemm_bf16_t h, Plan &pl)
+{
+    int rc;
+    // the small operand is B when N is small enough (D's rows are then the
+    // accumulator's rows), else A (D is the accumulator transposed)
+    const bool transposed = pl.N > kThinMaxRows;
+    const int64_t small = transposed ? pl.M : pl.N;
+    const int64_t large = transposed ? pl.N : pl.M;
+    pl.thin_nt = thin_nt(small);
+    pl.thin_transposed = transposed;
+    pl.pipeline = GEMM_BF16_PIPE_WS;
+    pl.cta_group = 1;
+    pl.persistent = 1;
+    pl.acc_buffers = 2;
+    pl.setmaxnreg = 0;
+    pl.stage_group = 1;
+    pl.epi_pingpong = 0;
+    pl.sched_dynamic = 0;
+    pl.k_order = 0;
+    pl.serpentine = 0;
+    pl.raster_group = 0;
+    pl.num_k_blocks = (int)((pl.K + kBlockK - 1) / kBlockK);
+    pl.tiles = (large + kBlockM - 1) / kBlockM;
+    pl.num_m_blocks = (int)pl.tiles;
+    pl.num_n_blocks = 1;
+    pl.thin_units = pl.tiles * pl.num_k_blocks;
+    pl.watchdog_ns = std::max<uint64_t>(pl.watchdog_ns, (uint64_t)pl.num_k_blocks * kWatchdogNsPerKBlock);
+    pl.stages = 0;
+    for (int s = kThinMaxStages; s >= 2; --s)
+        if (thin_smem_bytes(pl.thin_nt, s) <= h->max_smem_optin) {
+            pl.stages = s;
+            break;
+        }
+    if (pl.stages < 2)
+        return GEMM_BF16_ERR_UNSUPPORTED;
+    pl.smem = thin_smem_bytes(pl.thin_nt, pl.stages);
+    pl.fn = thin_kernel(pl.thin_nt);
+    pl.threads = kThinThreads;
+    if ((rc = prepare_kernel(pl.fn, h->max_smem_optin, &pl.regs)) != GEMM_BF16_OK)
+        return rc;
+    pl.grid_ctas = (int)std::min<int64_t>(std::min<int64_t>(h->num_sms, kThinMaxGrid), pl.thin_units);
+    pl.sk_tiles = pl.sk_head = pl.sk_pieces = 0;
+    pl.sk_units = 0;
+    pl.sk_slots = 0;
+    // two partial slots per CTA (thin_split.h) and a counter per tile; counters
+    // start at 0 and carry the launch's epoch, so a fresh allocation is zeroed
+    // and never reset afterwards
+    const size_t floats = (size_t)2 * (size_t)pl.grid_ctas * kBlockM * (size_t)pl.thin_nt;
+    if (floats > h->thin_ws_floats) {
+        float *nws = nullptr;
+        if (cudaMalloc(&nws, floats * sizeof(float)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_BF16_ERR_CUDA;
+        }
+        if (h->thin_ws)
+            cudaFree(h->thin_ws);
+        h->thin_ws = nws;
+        h->thin_ws_floats = floats;
+    }
+    if ((size_t)pl.tiles > h->thin_cnt_n) {
+        uint32_t *nc = nullptr;
+        if (cudaMalloc(&nc, (size_t)pl.tiles * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(nc, 0, (size_t)pl.tiles * sizeof(uint32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            if (nc)
+                cudaFree(nc);
+            return GEMM_BF16_ERR_CUDA;
+        }
+        if (h->thin_cnt)
+            cudaFree(h->thin_cnt);
+        h->thin_cnt = nc;
+        h->thin_cnt_n = (size_t)pl.tiles;
+    }
+    return GEMM_BF16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+GEMM_BF16_API const char *gemm_bf16_strerror(int status)
+{
+    switch (status) {
+    case GEMM_BF16_OK: return "ok";
+    case GEMM_BF16_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_BF16_ERR_ALIGNMENT: return "alignment: TMA needs 16-byte aligned bases and row strides";
+    case GEMM_BF16_ERR_NOT_PLANNED: return "not planned: call gemm_bf16_plan first";
+    case GEMM_BF16_ERR_CUDA: return "a CUDA runtime call failed";
+    case GEMM_BF16_ERR_TENSORMAP: return "TMA tensor-map encoding failed";
+    case GEMM_BF16_ERR_DEVICE_TIMEOUT: return "device watchdog: a barrier wait ran out and the kernel returned early";
+    case GEMM_BF16_ERR_UNSUPPORTED: return "unsupported device or option combination";
+    default: return "unknown status";
+    }
+}
+
+GEMM_BF16_API const char *gemm_bf16_version(void) { return "gemm_bf16 1.0 sm_103a"; }
+
+GEMM_BF16_API int gemm_bf16_check_problem(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd)
+{
+    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (lda < K || ldb < K || ldd < N)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if (lda > (int64_t(1) << 38) || ldb > (int64_t(1) << 38) || ldd > (int64_t(1) << 38))
+        return GEMM_BF16_ERR_INVALID_ARG;
+    if ((lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0)
+        return GEMM_BF16_ERR_ALIGNMENT;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_create(int device, gemm_bf16_t *out)
+{
+    if (!out)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    *out = nullptr;
+    int dev = device;
+    if (dev < 0 && cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || dev >= count) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    if (cudaSetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    int major = 0, minor = 0, sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3)
+        return GEMM_BF16_ERR_UNSUPPORTED;
+    gemm_bf16_t h = new (std::nothrow) gemm_bf16();
+    if (!h)
+        return GEMM_BF16_ERR_CUDA;
+    h->device = dev;
+    h->num_sms = sms;
+    h->max_smem_optin = (size_t)optin;
+    for (int k = 0; k < kNumOptions; ++k)
+        h->opt[k] = default_option(k);
+    if (cudaMalloc(&h->d_err, 4 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        if (h->d_err)
+            cudaFree(h->d_err);
+        delete h;
+        return GEMM_BF16_ERR_CUDA;
+    }
+    *out = h;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_destroy(gemm_bf16_t h)
+{
+    if (!h)
+        return GEMM_BF16_OK;
+    cudaSetDevice(h->device);
+    if (h->d_err)
+        cudaFree(h->d_err);
+    if (h->ws)
+        cudaFree(h->ws);
+    if (h->ws_flags)
+        cudaFree(h->ws_flags);
+    if (h->pack)
+        cudaFree(h->pack);
+    if (h->thin_ws)
+        cudaFree(h->thin_ws);
+    if (h->thin_cnt)
+        cudaFree(h->thin_cnt);
+    delete h;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_set_option(gemm_bf16_t h, int key, int64_t value)
+{
+    if (!h || key < 1 || key >= kNumOptions || !option_in_range(key, value))
+        return GEMM_BF16_ERR_INVALID_ARG;
+    h->opt[key] = value;
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_get_option(gemm_bf16_t h, int key, int64_t *value)
+{
+    if (!h || !value || key < 1 || key >= kNumOptions)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    *value = h->opt[key];
+    return GEMM_BF16_OK;
+}
+
+GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                 int64_t ldd)
+{
+    if (!h)
+        return GEMM_BF16_ERR_INVALID_ARG;
+    h->plan.valid = false;
+    h->maps_valid = false;
+    int rc = gemm_bf16_check_problem(M, N, K, lda, ldb, ldd);
+    if (rc != GEMM_BF16_OK)
+        return rc;
+    if ((rc = set_device(h)) != GEMM_BF16_OK)
+        return rc;
+
+    Plan pl;
+    pl.M = M, pl.N = N, pl.K = K, pl.lda = lda, pl.ldb = ldb, pl.ldd = ldd;
+    pl.pipeline = (int)h->opt[GEMM_BF16_OPT_PIPELINE];
+    pl.persistent = (int)h->opt[GEMM_BF16_OPT_PERSISTENT];
+    pl.acc_buffers = (int)h->opt[GEMM_BF16_OPT_ACC_BUFFERS];
+    pl.setmaxnreg = (int)h->opt[GEMM_BF16_OPT_SETMAXNREG];
+    pl.raster_group = (int)h->opt[GEMM_BF16_OPT_RASTER_GROUP];
+    pl.epilogue_opt = (int)h->opt[GEMM_BF16_OPT_EPILOGUE];
+    pl.epi_pingpong = (int)h->opt[GEMM_BF16_OPT_EPI_SCHEDULE];
+    pl.sched_dynamic = (int)h->opt[GEMM_BF16_OPT_SCHEDULER];
+    pl.k_order = (int)h->opt[GEMM_BF16_OPT_K_ORDER];
+    pl.serpentine = (int)h->opt[GEMM_BF16_OPT_SERPENTINE];
+    pl.fault_skip = (int)h->opt[GEMM_BF16_OPT_FAULT_SKIP_LOAD];
+    pl.watchdog_ns = (uint64_t)h->opt[GEMM_BF16_OPT_WATCHDOG_NS];
+    pl.epi_tma_allowed = ((ldd * 2) % 16) == 0;
+
+    // the thin kernel for decode-like shapes, else the square kernel
+    const int64_t thin_opt = h->opt[GEMM_BF16_OPT_THIN];
+    const bool square_defaults =
+        h->opt[GEMM_BF16_OPT_PIPELINE] == GEMM_BF16_PIPE_WS && h->opt[GEMM_BF16_OPT_CTA_GROUP] == 0 &&
+        h->opt[GEMM_BF16_OPT_PERSISTENT] == 1 && h->opt[GEMM_BF16_OPT_ACC_BUFFERS] == 2 &&
+        h->opt[GEMM_BF16_OPT_SETMAXNREG] == 0 && h->opt[GEMM_BF16_OPT_STAGES] == 0 &&
+        h->opt[GEMM_BF16_OPT_EPILOGUE] == 0 && h->opt[GEMM_BF16_OPT_MAX_CTAS] == 0 &&
+        h->opt[GEMM_BF16_OPT_STAGE_GROUP] == 0 && h->opt[GEMM_BF16_OPT_EPI_SCHEDULE] == 0 &&
+        h->opt[GEMM_BF16_OPT_SCHEDULER] == 0;
+    // automatic: where the thin kernel measured faster on GB300 (one operand of
+    // at most 32 rows streamed against >= 4096 rows of the other, K >= 1024:
+    // +2-8 %, and +40 % at M = 1); with 64 rows it was slower
+    const bool thin_auto_shape = std::min(M, N) <= 32 && std::max(M, N) >= 4096 && K >= 1024;
+    const bool thin = std::min(M, N) <= kThinMaxRows &&
+                      (thin_opt == 2 || (thin_opt == 1 && square_defaults && thin_auto_shape));
+    if ((rc = thin ? plan_thin(h, pl) : plan_square(h, pl)) != GEMM_BF16_OK)
+        return rc;
     // Operand repacking: a row pitch that is not a multiple of 128 bytes makes
     // every TMA box row straddle two L2 lines (~28% slower GEMM, measured).  A
     // copy costs one HBM read + write of the operand, i.e. time ~ rows * K,
@@ -650,7 +770,7 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->sk_head = p.sk_head;
     info->sk_slots = (int32_t)p.sk_slots;
     info->tile_m = kBlockM * p.cta_group;
-    info->tile_n = kBlockN;
+    info->tile_n = p.thin_nt ? p.thin_nt : kBlockN;
     info->tile_k = kBlockK;
     info->smem_bytes = (int32_t)p.smem;
     info->num_sms = h->num_sms;
@@ -663,6 +783,7 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->packed_ld = (int32_t)p.ldp;
     info->k_order = p.k_order;
     info->serpentine = p.serpentine;
+    info->thin = p.thin_nt;
     return GEMM_BF16_OK;
 }
 
@@ -676,6 +797,130 @@ struct FusedArgs {
     const void *bias;
     float alpha, beta;
 };
+
+// A launch's epoch: never 0 (the square kernel's flags start at 0) and never 0
+// in the 23 bits the thin kernel's counters keep.
+void next_epoch(gemm_bf16_t h)
+{
+    do
+        ++h->epoch;
+    while ((h->epoch & (0xFFFFFFFFu >> kThinCountBits)) == 0u);
+}
+
+// The operands as run_impl resolved them: the caller's pointers, and the ones
+// the kernel reads (the packed copies where the plan repacks).
+struct OperandView {
+    const void *A, *B;    // caller's
+    const void *Ae, *Be;  // read by the GEMM
+    int64_t lda_e, ldb_e;
+    void *pack_a, *pack_b;
+};
+
+int launch_repacks(gemm_bf16_t h, const OperandView &ops, cudaStream_t st)
+{
+    const Plan &pl = h->plan;
+    if (!ops.pack_a && !ops.pack_b)
+        return GEMM_BF16_OK;
+    RepackJob jobs[2];
+    int nj = 0;
+    if (ops.pack_a)
+        jobs[nj++] = {ops.A, ops.pack_a, pl.lda, pl.ldp, pl.M, pl.K};
+    if (ops.pack_b)
+        jobs[nj++] = {ops.B, ops.pack_b, pl.ldb, pl.ldp, pl.N, pl.K};
+    return launch_repack(jobs, nj, h->num_sms, st) != 0 ? GEMM_BF16_ERR_CUDA : GEMM_BF16_OK;
+}
+
+// One launch of the thin kernel (plan_thin): tensor maps of the large operand
+// (box 64 x 128) and the small one (box 64 x thin_nt), then the launch.
+int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz, cudaStream_t st, bool fault_maps)
+{
+    const Plan &pl = h->plan;
+    int rc;
+    const void *large = pl.thin_transposed ? ops.Be : ops.Ae;
+    const void *small = pl.thin_transposed ? ops.Ae : ops.Be;
+    const int64_t large_rows = pl.thin_transposed ? pl.N : pl.M;
+    const int64_t small_rows = pl.thin_transposed ? pl.M : pl.N;
+    const int64_t ld_large = pl.thin_transposed ? ops.ldb_e : ops.lda_e;
+    const int64_t ld_small = pl.thin_transposed ? ops.lda_e : ops.ldb_e;
+    if (fault_maps || !h->maps_valid || h->mA != ops.Ae || h->mB != ops.Be) {
+        if (fault_maps) {
+            h->maps_valid = false;
+            return GEMM_BF16_ERR_TENSORMAP;
+        }
+        if ((rc = encode_2d(&h->tmA, large, (uint64_t)pl.K, (uint64_t)large_rows, (uint64_t)ld_large * 2, kBlockK,
+                            kBlockM)) ||
+            (rc = encode_2d(&h->tmB, small, (uint64_t)pl.K, (uint64_t)small_rows, (uint64_t)ld_small * 2, kBlockK,
+                            (uint32_t)pl.thin_nt))) {
+            h->maps_valid = false;
+            return rc;
+        }
+        h->mA = ops.Ae, h->mB = ops.Be, h->mD = nullptr;
+        h->maps_valid = true;
+    }
+    if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK)
+        return rc;
+
+    ThinParams tp;
+    tp.rows = (int32_t)large_rows;
+    tp.thin = (int32_t)small_rows;
+    tp.num_k_blocks = pl.num_k_blocks;
+    tp.num_tiles = (int32_t)pl.tiles;
+    tp.units = pl.thin_units;
+    tp.stages = pl.stages;
+    tp.transposed = pl.thin_transposed ? 1 : 0;
+    tp.d_vec = ((reinterpret_cast<uintptr_t>(D) & 15u) == 0 && pl.ldd % 8 == 0) ? 1 : 0;
+    tp.fault_skip_it = pl.fault_skip;
+    tp.ldd = pl.ldd;
+    tp.D = D;
+    tp.err = h->d_err;
+    tp.watchdog_ns = pl.watchdog_ns;
+    tp.partials = h->thin_ws;
+    tp.counters = h->thin_cnt;
+    next_epoch(h);
+    tp.epoch = h->epoch;
+    tp.C = nullptr;
+    tp.bias = nullptr;
+    tp.ldc = 0;
+    tp.alpha = 1.f;
+    tp.beta = 0.f;
+    tp.fused = 0;
+    if (fz) {
+        tp.fused = kFusedOn;
+        tp.alpha = fz->alpha;
+        tp.beta = fz->beta;
+        if (fz->C) {
+            tp.C = fz->C;
+            tp.ldc = fz->ldc;
+            tp.fused |= kFusedC;
+        }
+        if (fz->bias) {
+            tp.bias = fz->bias;
+            tp.fused |= kFusedBias;
+        }
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    unsigned nattr = 0;
+    cfg.gridDim = dim3((unsigned)pl.grid_ctas, 1, 1);
+    cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    if (h->opt[GEMM_BF16_OPT_PDL]) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cfg.attrs = nattr ? attr : nullptr;
+    cfg.numAttrs = nattr;
+    void *args[3] = {&h->tmA, &h->tmB, &tp};
+    if (cudaLaunchKernelExC(&cfg, pl.fn, args) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    h->last_stream = st;
+    return GEMM_BF16_OK;
+}
 
 int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedArgs *fz, void *stream)
 {
@@ -714,6 +959,10 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
 
     // test hook: the encode fails as a driver error would, before any launch
     const bool fault_maps = h->opt[GEMM_BF16_OPT_FAULT_TENSORMAP] != 0;
+    if (pl.thin_nt) {
+        const OperandView ops = {A, B, Ae, Be, lda_e, ldb_e, pack_a, pack_b};
+        return run_thin(h, ops, D, fz, st, fault_maps);
+    }
     if (fault_maps || !h->maps_valid || h->mA != Ae || h->mB != Be || h->mD != D) {
         if (fault_maps) {
             h->maps_valid = false;
@@ -736,15 +985,10 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
         h->mA = Ae, h->mB = Be, h->mD = D;
         h->maps_valid = true;
     }
-    if (pack_a || pack_b) {
-        RepackJob jobs[2];
-        int nj = 0;
-        if (pack_a)
-            jobs[nj++] = {A, pack_a, pl.lda, pl.ldp, pl.M, pl.K};
-        if (pack_b)
-            jobs[nj++] = {B, pack_b, pl.ldb, pl.ldp, pl.N, pl.K};
-        if (launch_repack(jobs, nj, h->num_sms, st) != 0)
-            return GEMM_BF16_ERR_CUDA;
+    {
+        const OperandView ops = {A, B, Ae, Be, lda_e, ldb_e, pack_a, pack_b};
+        if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK)
+            return rc;
     }
 
     GemmParams prm;
@@ -771,8 +1015,7 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
     prm.sk_pieces = pl.sk_pieces;
     prm.workspace = pl.sk_tiles ? h->ws : nullptr;
     prm.flags = pl.sk_tiles ? h->ws_flags : nullptr;
-    if (++h->epoch == 0)
-        h->epoch = 1;
+    next_epoch(h);
     prm.epoch = h->epoch;
     prm.C = nullptr;
     prm.bias = nullptr;
@@ -904,8 +1147,11 @@ GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail)
     // Clearing the whole block also puts the tile counter back to 0: after a
     // watchdog give-up it is the only thing that does (normally the last SM
     // pair of each launch resets it).
+    // After a give-up the thin kernel's tile counters may hold a partial count;
+    // they go back to zero with the status word.
     if (cudaMemcpy(&w, h->d_err, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess ||
         (w != 0 && cudaMemset(h->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) ||
+        (w != 0 && h->thin_cnt && cudaMemset(h->thin_cnt, 0, h->thin_cnt_n * sizeof(uint32_t)) != cudaSuccess) ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;

@@ -94,11 +94,54 @@ inline size_t nows_smem_bytes(int stages)
     return 1024 + (size_t)stages * stage + 4 * (size_t)kStagingBytes + 256;
 }
 
+// The thin kernel (gemm_thin.cuh): one operand has at most 64 rows.  The
+// other ("large") operand is cut into 128-row tiles, each a tcgen05.mma M side,
+// and the small one is the MMA's N side, rounded up to kThinN (16, 32, 48 or 64).
+constexpr int kThinThreads = 256;  // warp 0 producer, 1 MMA, 2 TMEM allocation, 4-7 epilogue
+constexpr int kThinMaxStages = 12;
+constexpr int kThinMaxRows = 64;
+
+struct ThinParams {
+    int32_t rows;           // rows of the large operand
+    int32_t thin;           // rows of the small operand (1..64)
+    int32_t num_k_blocks;   // ceil(K / 64)
+    int32_t num_tiles;      // ceil(rows / 128)
+    int64_t units;          // num_tiles * num_k_blocks, split among the CTAs (thin_split.h)
+    int32_t stages;
+    int32_t transposed;     // 1: the large operand is B, so D[m][n] is accumulator row n, column m
+    int32_t d_vec;          // 1: rows of D are 16-byte aligned (vector stores, not transposed only)
+    int32_t fault_skip_it;  // test hook, -1 = off
+    int64_t ldd;
+    void *D;
+    uint32_t *err;
+    uint64_t watchdog_ns;
+    float *partials;        // 2 slots per CTA, 128 x NT fp32 each
+    uint32_t *counters;     // one per tile (thin_count_after)
+    uint32_t epoch;         // this launch's value (never 0)
+    // fused epilogue, as in GemmParams
+    const void *C;
+    const void *bias;
+    int64_t ldc;
+    float alpha, beta;
+    uint32_t fused;
+};
+
+inline int thin_nt(int64_t thin_rows) { return (int)((thin_rows + 15) / 16 * 16); }
+
+inline size_t thin_stage_bytes(int nt) { return (size_t)kBlockM * kBlockK * 2 + (size_t)nt * kBlockK * 2; }
+
+inline size_t thin_smem_bytes(int nt, int stages)
+{
+    return 1024 /* alignment slack */ + (size_t)stages * thin_stage_bytes(nt) + 512 /* barriers, tmem slot, flags */;
+}
+
 // Kernel entry points, one per compiled variant.  All take
 // (CUtensorMap A, CUtensorMap B, CUtensorMap D, GemmParams).
 const void *ws_kernel_c1(bool setmaxnreg);
 const void *ws_kernel_c2(bool setmaxnreg);
 const void *nows_kernel(bool mbar_war);
+// (CUtensorMap large, CUtensorMap small, ThinParams); nt = 16, 32, 48 or 64.
+const void *thin_kernel(int nt);
 
 // One operand copy: `rows` rows of `cols` bf16 from pitch ld_src to pitch
 // ld_dst (elements; both multiples of 8, both bases 16-byte aligned).

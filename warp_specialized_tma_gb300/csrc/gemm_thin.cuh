@@ -1,0 +1,358 @@
+// The thin kernel: D = A * B^T when one of M, N is at most 64 (decode-like
+// problems).  Such problems are bound by streaming the large operand from
+// HBM, not by the tensor pipe.  In the square kernel a 64-row operand would
+// still fill a 128-row MMA side, and 7/8 or more of its shared-memory stage
+// would hold TMA's zero fill.  Here the large operand takes the 128-row M
+// side of each tcgen05.mma.  The small operand is the N side, rounded up to
+// NT = 16..64, so a stage is 16 KiB of the large operand plus NT x 128 bytes.
+// The ring is then up to 12 stages deep and keeps ~2x the bytes in flight per
+// SM.
+//
+// One CTA per SM, no clusters.  Roles:
+//   warp 0, lane 0   TMA producer: for each of the CTA's items, per k-block:
+//                    wait "empty", expect_tx, load the large tile (64 x 128)
+//                    and the small one (64 x NT)
+//   warp 1, lane 0   MMA issuer: four tcgen05.mma (K = 16) per k-block into one
+//                    of two NT-column tensor-memory accumulators, commit ->
+//                    "empty"; after an item, commit -> accumulator full
+//   warp 2           allocates (and frees) tensor memory
+//   warps 4-7        epilogue: tensor memory -> registers; whole tiles are
+//                    stored directly, pieces of split tiles leave an fp32
+//                    partial, and the last piece to finish adds the others and
+//                    stores the tile (thin_split.h)
+// Every wait is bounded by the watchdog (WaitCtl in ptx.cuh).
+#pragma once
+
+#include "gemm_kernels.h"
+#include "ptx.cuh"
+#include "ring_index.h"
+#include "thin_split.h"
+
+namespace wstma {
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32_thin(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Counts this piece of tile t; true when it is the tile's last piece.
+__device__ __forceinline__ bool thin_arrive(uint32_t *counter, uint32_t epoch, uint32_t pieces)
+{
+    uint32_t cur = ld_acquire_gpu_u32_thin(counter);
+    for (;;) {
+        const uint32_t nv = thin_count_after(cur, epoch);
+        const uint32_t prev = atomicCAS(counter, cur, nv);
+        if (prev == cur)
+            return (nv & kThinCountMask) == pieces;
+        cur = prev;
+    }
+}
+
+// fp32 accumulator element -> the stored value (fused: alpha * acc + beta * C + bias).
+__device__ __forceinline__ float thin_epilogue_value(float acc, int64_t m, int64_t n, const ThinParams &p)
+{
+    if (!p.fused)
+        return acc;
+    float c = 0.f, b = 0.f;
+    if (p.fused & kFusedC)
+        c = __uint_as_float((uint32_t)(static_cast<const uint16_t *>(p.C)[m * p.ldc + n]) << 16);
+    if (p.fused & kFusedBias)
+        b = __uint_as_float((uint32_t)(static_cast<const uint16_t *>(p.bias)[n]) << 16);
+    return fmaf(p.alpha, acc, fmaf(p.beta, c, b));
+}
+
+__device__ __forceinline__ uint16_t thin_bf16(float f)
+{
+    return (uint16_t)(pack_bf16x2(__float_as_uint(f), 0u) & 0xFFFFu);
+}
+
+// Stores one accumulator row (this thread's row r of the large operand's tile)
+// to D.  Not transposed: D[r][0 .. thin).  Transposed: D[0 .. thin)[r], so the
+// 32 lanes of a warp store 32 consecutive elements of one row of D.
+template <int NT>
+__device__ __forceinline__ void thin_store_row(const float (&v)[NT], int64_t r, const ThinParams &p)
+{
+    if (r >= p.rows)
+        return;
+    uint16_t *const D = static_cast<uint16_t *>(p.D);
+    if (p.transposed) {
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+            if (i < p.thin)
+                D[(int64_t)i * p.ldd + r] = thin_bf16(thin_epilogue_value(v[i], i, r, p));
+        return;
+    }
+    uint16_t *const row = D + r * p.ldd;
+    if (p.d_vec && !p.fused && p.thin == NT) {
+#pragma unroll
+        for (int i = 0; i < NT; i += 8) {
+            uint4 q;
+            q.x = pack_bf16x2(__float_as_uint(v[i]), __float_as_uint(v[i + 1]));
+            q.y = pack_bf16x2(__float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
+            q.z = pack_bf16x2(__float_as_uint(v[i + 4]), __float_as_uint(v[i + 5]));
+            q.w = pack_bf16x2(__float_as_uint(v[i + 6]), __float_as_uint(v[i + 7]));
+            *reinterpret_cast<uint4 *>(row + i) = q;
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+        if (i < p.thin)
+            row[i] = thin_bf16(thin_epilogue_value(v[i], r, i, p));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThinThreads, 1)
+    gemm_thin_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmS,
+                     const ThinParams p)
+{
+    static_assert(NT % 16 == 0 && NT >= 16 && NT <= kThinMaxRows, "NT: 16, 32, 48 or 64");
+    constexpr uint32_t kLBytes = (uint32_t)kBlockM * kBlockK * 2;  // 128 rows of the large operand
+    constexpr uint32_t kSBytes = (uint32_t)NT * kBlockK * 2;       // NT rows of the small one
+    constexpr uint32_t kStageBytes = kLBytes + kSBytes;             // a multiple of 1024
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kBlockM, NT);
+    constexpr uint32_t kAllocCols = 2 * NT <= 32 ? 32u : (2 * NT <= 64 ? 64u : 128u);
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int S = p.stages;
+    const uint32_t stage0 = base;
+    const uint32_t full_bar = base + (uint32_t)S * kStageBytes;
+    const uint32_t empty_bar = full_bar + 8u * S;
+    const uint32_t accf_bar = empty_bar + 8u * S;
+    const uint32_t acce_bar = accf_bar + 16u;
+    const uint32_t done_bar = acce_bar + 16u;
+    const uint32_t tmem_slot = done_bar + 8u;
+    const uint32_t abort_flag = tmem_slot + 4u;
+    const uint32_t last_word = abort_flag + 4u;
+    const uint32_t go_words = last_word + 4u;  // 2 words, alternating by item
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar + 8u * s, 1);
+            mbar_init(empty_bar + 8u * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar + 8u * a, 1);
+            mbar_init(acce_bar + 8u * a, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(done_bar, 1);
+        st_shared_u32(abort_flag, 0u);
+        fence_mbarrier_init();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmL);
+        prefetch_tensormap(&tmS);
+    }
+    __syncthreads();
+    if (warp == 2) {
+        tmem_alloc<1>(tmem_slot, kAllocCols);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+    // Everything above touched only this CTA's shared and tensor memory.
+    grid_dependency_wait();
+
+    WaitCtl ctl;
+    ctl.abort_flag = abort_flag;
+    ctl.peer_abort_flag = 0u;
+    ctl.err = p.err;
+    ctl.set_limit(p.watchdog_ns);
+
+    const int32_t KB = p.num_k_blocks;
+    const int32_t G = (int32_t)gridDim.x;
+    const int32_t j = (int32_t)blockIdx.x;
+    const int64_t ub = thin_begin(p.units, G, j);
+    const int64_t ue = thin_begin(p.units, G, j + 1);
+    const int64_t t_first = ub / KB;
+    const int64_t t_last = (ue - 1) / KB;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int s = 0;
+        uint32_t ph = 0;
+        int32_t it = 0;
+        bool ok = true;
+        for (int64_t t = t_first; ok && t <= t_last; ++t) {
+            const int32_t kb0 = (int32_t)(ub > t * KB ? ub - t * KB : 0);
+            const int32_t kb1 = (int32_t)(ue < (t + 1) * KB ? ue - t * KB : KB);
+            const int32_t y = (int32_t)(t * kBlockM);
+            for (int32_t kb = kb0; kb < kb1; ++kb) {
+                if (!ctl.wait<false>(empty_bar + 8u * s, ring_empty_parity(ph), kRoleProducer, (uint32_t)s)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_bar + 8u * s;
+                const uint32_t sa = stage0 + (uint32_t)s * kStageBytes;
+                if (it != p.fault_skip_it) {
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    tma_load_2d(sa, &tmL, kb * kBlockK, y, fb);
+                    tma_load_2d(sa + kLBytes, &tmS, kb * kBlockK, 0, fb);
+                }
+                ++it;
+                ring_advance(s, ph, S);
+            }
+        }
+        grid_launch_dependents();
+        // Teardown: the last S loads may still be in flight if a role gave up.
+        const int32_t n = it < S ? it : S;
+        for (int32_t d = 1; d <= n; ++d) {
+            const int32_t i = it - d;
+            if (i == p.fault_skip_it)
+                continue;
+            ctl.wait_drain<false>(full_bar + 8u * (uint32_t)ring_stage_of(i, S), ring_parity_of(i, S),
+                                  (uint32_t)ring_stage_of(i, S));
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        const uint64_t ldesc0 = smem_desc_sw128(stage0);
+        const uint64_t sdesc0 = smem_desc_sw128(stage0 + kLBytes);
+        int s = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t acc_ph = 0;
+        bool ok = true;
+        for (int64_t t = t_first; ok && t <= t_last; ++t) {
+            const int32_t kb0 = (int32_t)(ub > t * KB ? ub - t * KB : 0);
+            const int32_t kb1 = (int32_t)(ue < (t + 1) * KB ? ue - t * KB : KB);
+            if (!ctl.wait<false>(acce_bar + 8u * acc, acc_ph ^ 1u, kRoleMmaAcc, (uint32_t)acc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NT);
+            for (int32_t kb = kb0; kb < kb1; ++kb) {
+                if (!ctl.wait<false>(full_bar + 8u * s, ring_full_parity(ph), kRoleMmaFull, (uint32_t)s)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint64_t step = (uint64_t)(((uint32_t)s * kStageBytes) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / 16; ++kk)
+                    mma_bf16<1>(d_tmem, ldesc0 + step + 2u * kk, sdesc0 + step + 2u * kk, kIdesc,
+                                (kb != kb0 || kk != 0) ? 1u : 0u);
+                mma_commit(empty_bar + 8u * s);
+                ring_advance(s, ph, S);
+            }
+            if (!ok)
+                break;
+            mma_commit(accf_bar + 8u * acc);
+            acc ^= 1;
+            if (acc == 0)
+                acc_ph ^= 1u;
+        }
+        // no MMA may still be writing tensor memory when it is freed
+        mma_commit(done_bar);
+        ctl.wait_drain<false>(done_bar, 0u, 0xFFFu);
+    } else if (warp >= 4) {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // tensor-memory lane quadrant
+        const int32_t row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_ph = 0;
+        uint32_t item_parity = 0;
+        for (int64_t t = t_first; t <= t_last; ++t) {
+            const int32_t kb0 = (int32_t)(ub > t * KB ? ub - t * KB : 0);
+            const int32_t kb1 = (int32_t)(ue < (t + 1) * KB ? ue - t * KB : KB);
+            // One thread waits for the accumulator and posts the outcome to all
+            // four warps, so that they all take the same branch; the posted word
+            // alternates with the item, so a warp one item behind reads its own.
+            const uint32_t go = go_words + 4u * item_parity;
+            item_parity ^= 1u;
+            if (threadIdx.x == 128)
+                st_volatile_shared_u32(
+                    go, ctl.wait<false>(accf_bar + 8u * acc, acc_ph, kRoleEpilogue, (uint32_t)acc) ? 1u : 0u);
+            named_barrier_sync(1u, 128u);
+            if (ld_volatile_shared_u32(go) == 0u)
+                break;
+            tc_fence_after_sync();
+            float v[NT];
+            {
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NT);
+                uint32_t r[16];
+#pragma unroll
+                for (int c = 0; c < NT / 16; ++c) {
+                    tmem_load_32x16(taddr + (uint32_t)(c * 16), r);
+                    tmem_load_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        asm volatile("" : "+r"(r[i])::"memory");
+                        v[c * 16 + i] = __uint_as_float(r[i]);
+                    }
+                }
+            }
+            // every read of this accumulator is done: hand it back to the MMA warp
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce_bar + 8u * acc);
+            acc ^= 1;
+            if (acc == 0)
+                acc_ph ^= 1u;
+
+            const int64_t r = t * kBlockM + row_in_tile;
+            if (kb0 == 0 && kb1 == KB) {
+                thin_store_row<NT>(v, r, p);  // this range holds the whole tile
+                continue;
+            }
+            // a piece of a split tile: leave the partial, count it, and let the
+            // last piece add every partial in range order and store the tile
+            float *const mine =
+                p.partials + ((size_t)thin_slot(p.units, G, KB, j, t) * kBlockM + (size_t)row_in_tile) * NT;
+#pragma unroll
+            for (int i = 0; i < NT; i += 4)
+                *reinterpret_cast<float4 *>(mine + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            __threadfence();
+            named_barrier_sync(1u, 128u);
+            const int32_t jf = thin_range_of(p.units, G, t * KB);
+            const int32_t jl = thin_range_of(p.units, G, (t + 1) * KB - 1);
+            if (threadIdx.x == 128)
+                st_volatile_shared_u32(last_word, thin_arrive(p.counters + t, p.epoch, (uint32_t)(jl - jf + 1)) ? 1u : 0u);
+            named_barrier_sync(1u, 128u);
+            if (ld_volatile_shared_u32(last_word) == 0u)
+                continue;
+            __threadfence();
+            float sum[NT];
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+                sum[i] = 0.f;
+            for (int32_t jj = jf; jj <= jl; ++jj) {
+                const float *part =
+                    p.partials + ((size_t)thin_slot(p.units, G, KB, jj, t) * kBlockM + (size_t)row_in_tile) * NT;
+#pragma unroll
+                for (int i = 0; i < NT; i += 4) {
+                    const float4 f = __ldcg(reinterpret_cast<const float4 *>(part + i));
+                    sum[i] += f.x;
+                    sum[i + 1] += f.y;
+                    sum[i + 2] += f.z;
+                    sum[i + 3] += f.w;
+                }
+            }
+            thin_store_row<NT>(sum, r, p);
+            // the next launch's first piece of this tile starts from zero
+            named_barrier_sync(1u, 128u);
+            if (threadIdx.x == 128)
+                p.counters[t] = 0u;
+        }
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, kAllocCols);
+    }
+}
+
+}  // namespace wstma

@@ -1,0 +1,61 @@
+// Work split of the thin kernel (gemm_thin.cuh), shared with the CPU check of
+// it (tests/thin_split_check.cpp).  Plain C++: no CUDA types.
+//
+// The large operand is cut into tiles of 128 rows, each of KB k-blocks, which
+// gives U = tiles * KB units.  CTA j of a grid of G (G <= U) takes the
+// contiguous units [begin(j), begin(j + 1)), begin(j) = j U / G, and every range
+// holds at least one unit.  A range covers whole tiles in its middle; its first
+// and its last tile may be partial, and so a range leaves at most two fp32
+// partials: slot 2j for its first tile and slot 2j + 1 for its last.  The
+// pieces of tile t are the ranges from range_of(t KB) to range_of((t + 1) KB - 1).
+// The last piece to finish adds the others' partials, in range order, and
+// stores the tile.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define WSTMA_THIN_FN __host__ __device__ __forceinline__
+#else
+#define WSTMA_THIN_FN inline
+#endif
+
+namespace wstma {
+
+WSTMA_THIN_FN int64_t thin_begin(int64_t U, int32_t G, int32_t j) { return (int64_t)j * U / G; }
+
+// The range that holds unit u (0 <= u < U).
+WSTMA_THIN_FN int32_t thin_range_of(int64_t U, int32_t G, int64_t u)
+{
+    int32_t j = (int32_t)(u * G / U);
+    while (j + 1 < G && thin_begin(U, G, j + 1) <= u)
+        ++j;
+    while (j > 0 && thin_begin(U, G, j) > u)
+        --j;
+    return j;
+}
+
+// Workspace slot of range j's partial of tile t (t is its first or its last tile).
+WSTMA_THIN_FN int32_t thin_slot(int64_t U, int32_t G, int32_t KB, int32_t j, int64_t t)
+{
+    return 2 * j + (t == thin_begin(U, G, j) / KB ? 0 : 1);
+}
+
+// Tile-completion counter: the launch's epoch in the high 23 bits, the pieces
+// that have arrived in the low 9.  A counter left by an older launch (another
+// epoch) counts as zero.  The host never uses an epoch whose low 23 bits are
+// zero, the last piece of a tile puts its counter back to zero, and after a
+// watchdog give-up the host clears the counters; so a count from a launch
+// 2^23 launches back, which would carry the same epoch bits, is never left.
+constexpr uint32_t kThinCountBits = 9;
+constexpr uint32_t kThinCountMask = (1u << kThinCountBits) - 1u;
+constexpr int32_t kThinMaxGrid = (int32_t)kThinCountMask;
+
+WSTMA_THIN_FN uint32_t thin_count_after(uint32_t cur, uint32_t epoch)
+{
+    const uint32_t ep = epoch & (0xFFFFFFFFu >> kThinCountBits);
+    const uint32_t have = (cur >> kThinCountBits) == ep ? (cur & kThinCountMask) : 0u;
+    return (ep << kThinCountBits) | (have + 1u);
+}
+
+}  // namespace wstma
