@@ -152,10 +152,10 @@ def test_thin_selection():
     with binding.Gemm(0) as g:  # automatic (the default)
         assert g.plan(16, 8192, 8192)["thin"] == 16
         assert g.plan(1, 8192, 8192)["thin"] == 16
-        assert g.plan(8192, 32, 1024)["thin"] == 32
-        assert g.plan(8192, 33, 8192)["thin"] == 0  # 48 or 64 rows: the square kernel measured faster
+        assert g.plan(8192, 16, 4096)["thin"] == 16
+        assert g.plan(8192, 17, 8192)["thin"] == 0  # 24-64 rows: the square kernel measured as fast or faster
         assert g.plan(16, 4000, 8192)["thin"] == 0  # too little to stream
-        assert g.plan(16, 8192, 1016)["thin"] == 0
+        assert g.plan(16, 8192, 4088)["thin"] == 0
         assert g.plan(8192, 8192, 8192)["thin"] == 0
     with binding.Gemm(0, thin=2) as g:
         assert g.plan(33, 33, 104)["thin"] == 48

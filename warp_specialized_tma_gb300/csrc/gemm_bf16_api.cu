@@ -704,10 +704,11 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         h->opt[GEMM_BF16_OPT_EPILOGUE] == 0 && h->opt[GEMM_BF16_OPT_MAX_CTAS] == 0 &&
         h->opt[GEMM_BF16_OPT_STAGE_GROUP] == 0 && h->opt[GEMM_BF16_OPT_EPI_SCHEDULE] == 0 &&
         h->opt[GEMM_BF16_OPT_SCHEDULER] == 0;
-    // automatic: where the thin kernel measured faster on GB300 (one operand of
-    // at most 32 rows streamed against >= 4096 rows of the other, K >= 1024:
-    // +2-8 %, and +40 % at M = 1); with 64 rows it was slower
-    const bool thin_auto_shape = std::min(M, N) <= 32 && std::max(M, N) >= 4096 && K >= 1024;
+    // automatic: where the thin kernel measured faster on GB300, one operand of
+    // at most 16 rows streamed against >= 4096 rows of the other with K >= 4096
+    // (+2-13 %, and +40 % at M = 1); with 24-64 small rows, or K <= 2048, it
+    // was as fast or slower
+    const bool thin_auto_shape = std::min(M, N) <= 16 && std::max(M, N) >= 4096 && K >= 4096;
     const bool thin = std::min(M, N) <= kThinMaxRows &&
                       (thin_opt == 2 || (thin_opt == 1 && square_defaults && thin_auto_shape));
     if ((rc = thin ? plan_thin(h, pl) : plan_square(h, pl)) != GEMM_BF16_OK)
