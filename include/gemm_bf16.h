@@ -249,8 +249,11 @@ GEMM_BF16_API int gemm_bf16_check_problem(int64_t M, int64_t N, int64_t K,
                                           int64_t lda, int64_t ldb, int64_t ldd);
 
 /* Validates the problem (as gemm_bf16_check_problem), resolves the options,
- * and picks the kernel, stage count, tile order and grid.  Re-planning a handle
- * is allowed and replaces the previous plan.  Launches nothing. */
+ * and picks the kernel (the square SM-pair kernel, or the thin kernel of
+ * GEMM_BF16_OPT_THIN), stage count, tile order and grid.  Allocates (or grows)
+ * the handle's device scratch the plan needs: the stream-K workspace, the thin
+ * kernel's partials and tile counters, the packed operand copies.  Re-planning
+ * a handle is allowed and replaces the previous plan.  Launches nothing. */
 GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
                                  int64_t lda, int64_t ldb, int64_t ldd);
 
@@ -259,7 +262,8 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
 
 /* Enqueues D = A * B^T on `stream` and returns without synchronising.
  * Launches of one handle share its device scratch (stream-K workspace, tile
- * counter, packed operand copies): do not let two launches of the same handle
+ * counter, thin-kernel partials and counters, packed operand copies): do not
+ * let two launches of the same handle
  * run at the same time (e.g. on two streams without an ordering between them);
  * use one handle per stream instead.  When the plan repacks an operand
  * (plan_info.repack) a copy kernel runs on `stream` before the GEMM.
