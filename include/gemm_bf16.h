@@ -316,10 +316,11 @@ GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail);
  * exactly like gemm_bf16_run with the default
  * options (same arguments and alignment rules, same kernel), with A, B, D and
  * the stream supplied by the caller, and allocates nothing -- no cudaMalloc,
- * cudaFree or allocating library call.  Two parts of the default plan need
+ * cudaFree or allocating library call.  Three parts of the default plan need
  * device memory of their own and are left out: stream-K (every tile runs
- * whole) and operand repacking (a row pitch that is not a multiple of 128
- * bytes is read in place, at the slower rate).
+ * whole), operand repacking (a row pitch that is not a multiple of 128 bytes
+ * is read in place, at the slower rate) and the thin kernel (decode-like
+ * shapes run on the square kernel).
  *
  * Its scratch (the kernel watchdog's status word, 4 bytes) lives in a fixed
  * 256-byte device array inside the library that every GPU loading the library
