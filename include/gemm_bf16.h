@@ -312,15 +312,20 @@ GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail);
  * pages: this is a property of the library's interface, not of the method).
  * Runtimes whose pool owns all device memory, and loops that cannot afford an
  * allocation's synchronisation, cannot call gemm_bf16_create (it allocates);
- * they call this instead.  It keeps no handle: it computes D = A * B^T
- * exactly like gemm_bf16_run with the default
- * options (same arguments and alignment rules, same kernel), with A, B, D and
- * the stream supplied by the caller, and allocates nothing -- no cudaMalloc,
- * cudaFree or allocating library call.  Three parts of the default plan need
- * device memory of their own and are left out: stream-K (every tile runs
- * whole), operand repacking (a row pitch that is not a multiple of 128 bytes
- * is read in place, at the slower rate) and the thin kernel (decode-like
- * shapes run on the square kernel).
+ * they call this instead.  It keeps no handle: it computes D = A * B^T with
+ * the same arguments, alignment rules and kernel (SM-pair tiles, deepest ring,
+ * persistent grid, grouped serpentine raster, alternating k direction) as
+ * gemm_bf16_run with the default options, with A, B, D and the stream
+ * supplied by the caller, and allocates nothing -- no cudaMalloc, cudaFree or
+ * allocating library call.  Parts of the default plan it leaves out: stream-K
+ * (it needs a partials workspace; every tile runs whole), operand repacking (it
+ * needs a packed copy; a row pitch that is not a multiple of 128 bytes is read
+ * in place, at the slower rate), the thin kernel (it needs a partials
+ * workspace; decode-like shapes run on the square kernel), and the
+ * programmatic-dependent-launch attribute (the launch waits for the previous
+ * work on the stream to finish before its prologue starts).  Its results
+ * differ from gemm_bf16_run's only in the fp32 summation order of the tiles
+ * that gemm_bf16_run splits (exact whenever every partial sum is).
  *
  * Its scratch (the kernel watchdog's status word, 4 bytes) lives in a fixed
  * 256-byte device array inside the library that every GPU loading the library
@@ -328,9 +333,14 @@ GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail);
  * is refused with INVALID_ARG before anything is enqueued.  Every call shares
  * the array: each call clears the status word on `stream` before its launch,
  * so calls that overlap on the GPU (different streams, or threads) race on it.
- * If `status` is not NULL, the status word after the kernel is copied there on
- * `stream` (0 = fine, else the watchdog word described at
- * gemm_bf16_device_status); it is valid once the stream has synchronised.
+ *
+ * `status` may be NULL.  Otherwise it must point to page-locked host memory
+ * (cudaHostAlloc / cudaHostRegister) or to device memory: the status word
+ * after the kernel (0 = fine, else the watchdog word described at
+ * gemm_bf16_device_status) is copied there on `stream`, asynchronously, and is
+ * valid once the stream has synchronised.  Pageable host memory would turn
+ * that copy into one that blocks the calling thread until the GEMM is done,
+ * so it is refused with INVALID_ARG before anything is enqueued.
  *
  * The first call on each device (with that device current) does a one-time
  * set-up: it looks up the array's device address, sets the kernel's shared-

@@ -71,8 +71,7 @@ _SIGNATURES = {
                                            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                            ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
     "gemm_bf16_device_status": (ctypes.c_int, [_H, ctypes.POINTER(ctypes.c_uint32)]),
-    "gemm_bf16_run_noalloc": (ctypes.c_int, [ctypes.c_int64] * 6 + [ctypes.c_void_p] * 4
-                              + [ctypes.POINTER(ctypes.c_uint32)]),
+    "gemm_bf16_run_noalloc": (ctypes.c_int, [ctypes.c_int64] * 6 + [ctypes.c_void_p] * 5),
     "gemm_bf16_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_bf16_version": (ctypes.c_char_p, []),
 }
@@ -200,13 +199,15 @@ def gemm_bf16_device_status(h):
     return st, w.value
 
 
-def gemm_bf16_run_noalloc(M, N, K, lda, ldb, ldd, A: int, B: int, D: int, stream: int = 0, status=None) -> int:
-    """Allocation-free GEMM on the current device; `status` may be a ctypes.c_uint32
-    that receives the watchdog word once the stream has synchronised."""
+def gemm_bf16_run_noalloc(M, N, K, lda, ldb, ldd, A: int, B: int, D: int, stream: int = 0,
+                          status: int | None = None) -> int:
+    """Allocation-free GEMM on the current device.  `status` is None or the
+    address of a uint32 in page-locked host memory or device memory, which
+    receives the watchdog word once the stream has synchronised."""
     return load().gemm_bf16_run_noalloc(int(M), int(N), int(K), int(lda), int(ldb), int(ldd),
                                         ctypes.c_void_p(A), ctypes.c_void_p(B), ctypes.c_void_p(D),
                                         ctypes.c_void_p(stream),
-                                        None if status is None else ctypes.byref(status))
+                                        None if status is None else ctypes.c_void_p(int(status)))
 
 
 def gemm_bf16_strerror(status: int) -> str:

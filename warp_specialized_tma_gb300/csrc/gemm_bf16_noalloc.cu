@@ -12,9 +12,10 @@
 //
 // It runs the same kernel as gemm_bf16_run with the default plan (SM-pair
 // 256x256 tiles, deepest ring, persistent grid, 1 s watchdog) except that every
-// tile runs whole: splitting tiles along k (stream-K) needs a partials
-// workspace of several MiB, which this entry point does not have.  It calls no
-// cudaMalloc, cudaFree or allocating library routine.
+// tile runs whole (splitting tiles along k, stream-K, needs a partials
+// workspace of several MiB), operands are read in place (repacking needs a
+// copy) and the launch carries no programmatic-dependent-launch attribute.  It
+// calls no cudaMalloc, cudaFree or allocating library routine.
 #include "gemm_bf16.h"
 
 #include <cuda.h>
@@ -36,6 +37,7 @@ namespace {
 // array's fixed capacity: 64 words = 256 bytes per device.
 constexpr int kScratchWordsNeeded = 1;
 constexpr int kScratchWordsMax = 64;
+static_assert(kScratchWordsNeeded <= kScratchWordsMax, "a call's scratch must fit the fixed array");
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWatchdogNs = 1000000000ull;
 constexpr uint64_t kWatchdogNsPerKBlock = 2000;  // no wait outlasts one tile's k-range of MMAs
@@ -161,9 +163,18 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
     if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
         (reinterpret_cast<uintptr_t>(D) & 1u))
         return GEMM_BF16_ERR_ALIGNMENT;
-    // the scratch this call needs must fit the fixed array
-    if (kScratchWordsNeeded > kScratchWordsMax)
-        return GEMM_BF16_ERR_INVALID_ARG;
+    // A pageable `status` would make the status copy block this thread until
+    // the GEMM is done (and cannot be captured): only page-locked host memory
+    // or device memory is taken.
+    if (status) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, status) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_BF16_ERR_INVALID_ARG;
+        }
+        if (pa.type != cudaMemoryTypeHost && pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged)
+            return GEMM_BF16_ERR_INVALID_ARG;
+    }
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
@@ -251,7 +262,7 @@ extern "C" GEMM_BF16_API int gemm_bf16_run_noalloc(int64_t M, int64_t N, int64_t
         return GEMM_BF16_ERR_CUDA;
     }
     if (status &&
-        cudaMemcpyAsync(status, ds->scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+        cudaMemcpyAsync(status, ds->scratch, sizeof(uint32_t), cudaMemcpyDefault, st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;
     }
