@@ -14,7 +14,9 @@ bf16 before the store).  Parity status: pinned (tests/test_oracle.py).
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -27,16 +29,29 @@ _lock = threading.Lock()
 _lib = None
 
 
+_STAMP = _LIB + ".stamp"
+_CMD = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def _stamp() -> str:
+    """The source's sha256, the host architecture and the compiler command: a
+    library built from other source or on another machine never matches."""
+    with open(_SRC, "rb") as fh:
+        digest = hashlib.sha256(fh.read()).hexdigest()
+    return f"{digest} machine={platform.machine()} cmd={' '.join(_CMD)}"
+
+
 def build(force: bool = False) -> str:
     """Compile gemm_oracle.c into liboracle.so (gcc, OpenMP, no fp contraction)."""
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
+    if not force and os.path.exists(_LIB) and os.path.exists(_STAMP):
+        with open(_STAMP) as fh:
+            if fh.read().strip() == _stamp():
+                return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC",
-           "-shared", "-o", tmp, _SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    subprocess.run(_CMD + ["-o", tmp, _SRC, "-lm"], check=True)
     os.replace(tmp, _LIB)
+    with open(_STAMP, "w") as fh:
+        fh.write(_stamp())
     return _LIB
 
 

@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -68,18 +69,35 @@ def _stamp_path() -> str:
     return os.path.join(BUILD_DIR, "stamp.txt")
 
 
-def up_to_date() -> bool:
+def _nvcc_version(cc: str) -> str:
+    try:
+        res = subprocess.run([cc, "--version"], capture_output=True, text=True)
+        return res.stdout.strip().splitlines()[-1] if res.stdout.strip() else "unknown"
+    except OSError:
+        return "unknown"
+
+
+def build_stamp(cc: str | None = None) -> str:
+    """What a built library depends on: its sources, the host architecture it
+    was linked for, the compiler and the flags.  A library built on another
+    machine (an x86_64 build seen on an aarch64 host) never matches."""
+    cc = cc or nvcc()
+    return "\n".join([source_digest(), "machine=" + platform.machine(), "nvcc=" + _nvcc_version(cc),
+                      "flags=" + " ".join(ARCH + FLAGS)])
+
+
+def up_to_date(cc: str | None = None) -> bool:
     if not os.path.exists(LIB) or not os.path.exists(_stamp_path()):
         return False
     with open(_stamp_path()) as fh:
-        return fh.read().strip() == source_digest()
+        return fh.read().strip() == build_stamp(cc)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+    cc = nvcc()
+    if not force and up_to_date(cc):
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
-    cc = nvcc()
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
@@ -103,7 +121,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
     os.replace(tmp, LIB)
     with open(_stamp_path(), "w") as fh:
-        fh.write(source_digest())
+        fh.write(build_stamp(cc))
     return LIB
 
 
