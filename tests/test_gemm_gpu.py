@@ -84,25 +84,6 @@ def _ordered(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
 
 
-def parity_stats(D, A, B, M, N, K, rows):
-    """Against the oracle on `rows`: errors vs the unrounded fp64 sum, the
-    tolerance count, and the exact-match fraction and ulp histogram vs the
-    oracle's bf16 rounding (a correct kernel differs from it only by rounding
-    flips and fp32 accumulation error, which matters most near zero)."""
-    ref64, refbf = oracle.gemm_rows(inputs.bits(A), inputs.bits(B), K=K, rows=rows)
-    got_bits = inputs.bits(D)[rows][:, :N]
-    got = inputs.from_bits(np.ascontiguousarray(got_bits)).double().numpy()
-    tol = 4e-3 * np.abs(ref64) + 2e-3 * math.sqrt(K) * rms(A, K) * rms(B, K)
-    err = np.abs(got - ref64)
-    ulp = np.abs(_ordered(got_bits) - _ordered(refbf))
-    big = np.abs(ref64) >= 0.25 * math.sqrt(K) * rms(A, K) * rms(B, K)  # a quarter of the typical size or more
-    return {"elements": int(err.size), "over_tolerance": int((~(err <= tol)).sum()),
-            "max_abs_err": float(err.max()), "max_err_over_tol": float((err / tol).max()),
-            "exact_frac": float((ulp == 0).mean()),
-            "ulp_hist": {str(k): int((ulp == k).sum()) for k in (0, 1, 2)} | {"3+": int((ulp >= 3).sum())},
-            "max_ulp_away_from_zero": int(ulp[big].max()) if big.any() else 0}
-
-
 def sample_rows(M: int, tile_m: int = 128, seed: int = 0, extra: int = 16):
     """First/last row of every 128-row slab plus random rows."""
     rng = np.random.default_rng(seed)
@@ -521,17 +502,63 @@ def test_identity_and_permutation_full_tiles():
 
 
 # ------------------------------------------------------------------ the five workloads
+def every_element(D, A, B, M, N, K, exact=False, band=1024):
+    """Every element of D against the oracle, computed in bands of rows (the
+    oracle's fp64 sums of one band at a time): the tolerance count, the exact
+    matches against the oracle's bf16 rounding and the ulp histogram.  With
+    `exact`, every element must equal the oracle's bf16 rounding bit for bit.
+    Padding columns n >= N must keep their sentinel."""
+    Ab, Bb = inputs.bits(A), inputs.bits(B)
+    Dbits = inputs.bits(D)
+    scale = math.sqrt(K) * rms(A, K) * rms(B, K)
+    st = {"elements": 0, "over_tolerance": 0, "mismatches": 0, "max_abs_err": 0.0, "max_err_over_tol": 0.0,
+          "ulp_hist": {"0": 0, "1": 0, "2": 0, "3+": 0}, "max_ulp_away_from_zero": 0}
+    first_bad = None
+    for r0 in range(0, M, band):
+        rows = np.arange(r0, min(M, r0 + band), dtype=np.int64)
+        ref64, refbf = oracle.gemm_rows(Ab, Bb, K=K, rows=rows)
+        got_bits = np.ascontiguousarray(Dbits[r0:r0 + rows.size, :N])
+        got = inputs.from_bits(got_bits).double().numpy()
+        tol = 4e-3 * np.abs(ref64) + 2e-3 * scale
+        err = np.abs(got - ref64)
+        over = ~(err <= tol)
+        mism = got_bits != refbf
+        if first_bad is None and (over.any() or (exact and mism.any())):
+            idx = np.argwhere(over | (mism if exact else over))[0]
+            first_bad = (int(r0 + idx[0]), int(idx[1]))
+        ulp = np.abs(_ordered(got_bits) - _ordered(refbf))
+        big = np.abs(ref64) >= 0.25 * scale  # a quarter of the typical magnitude or more
+        st["elements"] += int(err.size)
+        st["over_tolerance"] += int(over.sum())
+        st["mismatches"] += int(mism.sum())
+        st["max_abs_err"] = max(st["max_abs_err"], float(err.max()))
+        st["max_err_over_tol"] = max(st["max_err_over_tol"], float((err / tol).max()))
+        for k in (0, 1, 2):
+            st["ulp_hist"][str(k)] += int((ulp == k).sum())
+        st["ulp_hist"]["3+"] += int((ulp >= 3).sum())
+        if big.any():
+            st["max_ulp_away_from_zero"] = max(st["max_ulp_away_from_zero"], int(ulp[big].max()))
+    st["exact_frac"] = st["ulp_hist"]["0"] / max(st["elements"], 1)
+    st["first_bad"] = first_bad
+    assert st["elements"] == M * N
+    assert st["over_tolerance"] == 0, f"{st['over_tolerance']} elements outside tolerance, first {first_bad}"
+    if exact:
+        assert st["mismatches"] == 0, f"{st['mismatches']} mismatches, first at {first_bad}"
+    if Dbits.shape[1] > N:
+        assert np.all(Dbits[:, N:] == SENTINEL_BITS)
+    return st
+
+
 @pytest.mark.parametrize("name", list(inputs.WORKLOADS))
-def test_workload_sampled_rows(name):
+def test_workload_every_element(name):
+    # the full-size workload in the launch configuration bench.py times, every
+    # element of D against the oracle
     w = inputs.WORKLOADS[name]
     M, N, K = w["M"], w["N"], w["K"]
     A, B = inputs.make_workload(name)
     D = run_gpu(A, B, M, N, K)
-    rows = sample_rows(M) if M > 512 else np.arange(M)
-    check(D, A, B, M, N, K, rows=rows)
-    st = parity_stats(D, A, B, M, N, K, rows)
+    st = every_element(D, A, B, M, N, K)
     print(f"parity {name}: {st}")
-    assert st["over_tolerance"] == 0
     # away from zero the fp32 sum is far closer than a bf16 ulp to the exact
     # one, so the result is the oracle's rounding or its neighbour
     assert st["max_ulp_away_from_zero"] <= 1
@@ -539,12 +566,13 @@ def test_workload_sampled_rows(name):
 
 @pytest.mark.parametrize("name", list(inputs.WORKLOADS))
 def test_workload_integer_inputs_exact(name):
+    # same shapes and launch configuration, integer-valued inputs: every fp32
+    # partial sum is exact, so every element must be the oracle's bit for bit
     w = inputs.WORKLOADS[name]
     M, N, K = w["M"], w["N"], w["K"]
     A, B = inputs.make_problem(M, N, K, "int2", seed=w["seed"] + 100)
     D = run_gpu(A, B, M, N, K)
-    rows = sample_rows(M, seed=1, extra=8) if M > 512 else None
-    check(D, A, B, M, N, K, rows=rows, exact=True)
+    every_element(D, A, B, M, N, K, exact=True)
 
 
 def test_ragged_padded_ldd_uses_tma_store():
@@ -552,7 +580,7 @@ def test_ragged_padded_ldd_uses_tma_store():
     M, N, K = w["M"], w["N"], w["K"]
     A, B = inputs.make_workload("ragged")
     D = run_gpu(A, B, M, N, K, ldd=6000, epilogue=1)
-    check(D, A, B, M, N, K, rows=sample_rows(M, seed=2, extra=8))
+    every_element(D, A, B, M, N, K)
 
 
 def test_all_ones_full_size_property():
