@@ -18,7 +18,8 @@ Besides the headline workload, rank 0 at N = 1 reports in ``detail``:
              bounded sample of each;
   skinny     decode-like shapes (16 x 8192 x 8192, 8192 x 16 x 8192,
              64 x 8192 x 8192): compulsory HBM GB/s against the measured copy
-             bandwidth;
+             bandwidth, and against a device copy that moves the same bytes
+             (the rate HBM gives a plain streaming kernel at this size);
   sustained  the headline kernel back to back for >= 1.5 s under the power cap,
              with its SM clock.
 
@@ -444,7 +445,7 @@ def run_reference(args):
 
 
 def measure_shape(M, N, K, dist, seed, dev, stream, peaks, peak_src, flush_buf, label,
-                  cpu_seconds=None, graph_too=False):
+                  cpu_seconds=None, graph_too=False, hbm_comparator=False):
     """One problem through the C ABI: plan, warm up, time.  Inputs larger than
     L2 are timed back to back; smaller ones launch by launch with an L2 flush
     before each.  Returns a dict for the bench line's detail block."""
@@ -511,6 +512,19 @@ def measure_shape(M, N, K, dist, seed, dev, stream, peaks, peak_src, flush_buf, 
         "plan": {k: info[k] for k in ("cta_group", "grid_ctas", "stages", "tiles", "sk_tiles", "sk_head",
                                       "repack", "thin")},
     }
+    if hbm_comparator:
+        # A device copy that moves the same number of bytes (half the bytes
+        # read, half written) at this transfer size: what HBM delivers to a
+        # plain streaming kernel with the same fixed costs of a launch.
+        half = int(roof["bytes"] // 4)  # bf16 elements read = elements written = bytes / 4
+        src = torch.empty(half, dtype=torch.bfloat16, device=dev)
+        dst = torch.empty_like(src)
+        cms = time_back_to_back(lambda: dst.copy_(src), 20, stream, dev)
+        cgbs = 4.0 * half / (cms * 1e-3) / 1e9
+        out["copy_same_bytes"] = {"what": "dst.copy_(src) moving the same bytes (half read, half written), "
+                                          "back to back", "us": cms * 1e3, "gbs": cgbs,
+                                  "ours_over_copy": gbs / cgbs}
+        del src, dst
     if graph_us is not None:
         out["graph_replay_us_per_launch"] = graph_us
         out["graph_replay_note"] = "200 launches replayed from one CUDA graph, back to back (inputs stay in L2)"
@@ -728,7 +742,7 @@ def run_ours(args):
         skinny = {}
         for (m, n_, k) in SKINNY_SHAPES:
             skinny[f"{m}x{n_}x{k}"] = measure_shape(m, n_, k, "uniform", 3, dev, stream, peaks, peak_src,
-                                                    flush_buf, f"{m}x{n_}x{k}")
+                                                    flush_buf, f"{m}x{n_}x{k}", hbm_comparator=True)
 
     if dist.rank == 0:
         line = {
