@@ -443,49 +443,61 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             }
         }
         for (;;) {
-            // One thread per group finds the next item and polls the accumulator
-            // barrier, then posts both; the other warps sleep on a named barrier
-            // instead of polling (every poll competes with the MMA issuer).  The
-            // posted words alternate with the item parity, so a warp that is one
-            // item behind never reads the next item's words.
+            // One thread per group polls the accumulator barrier and posts the
+            // outcome; the other warps sleep on a named barrier instead of polling
+            // (every poll competes with the MMA issuer).  With the static schedule
+            // every epilogue thread walks the work sequence itself and prepares
+            // the item before the group meets, so that only the broadcast stands
+            // between the accumulator becoming ready and the first tensor-memory
+            // load; with the dynamic scheduler the poller also posts the item it
+            // took from the schedule ring.  The posted words alternate with the
+            // item parity, so a warp that is one item behind never reads the next
+            // item's words.
             const uint32_t go = go_area + 16u * (2u * (uint32_t)grp + tile_parity);
+            WorkItem w = {0, 0, 0};
+            uint32_t st = 1;  // 1 = drain item w, 2 = no more items, 0 = gave up
+            if (!dyn) {
+                if (!wi.next(w)) {
+                    st = 2;
+                } else if (pingpong) {
+                    WorkItem skip;  // the other group's item
+                    wi.next(skip);
+                }
+            }
+            TileCoord tc = {0, 0};
+            if (!dyn && st == 1u)
+                tc = tile_coord(w.tile, p);
             if (poller) {
-                WorkItem w = {0, 0, 0};
-                uint32_t st = 1;  // 1 = drain item w, 2 = no more items, 0 = gave up
-                if (lane == 0) {
-                    if (dyn) {
-                        if (!ring_get<kCluster>(ctl, ring, ring_full, leader_ring_empty, seq, w))
-                            st = 0;
-                        else if (w.tile < 0)
-                            st = 2;
-                    } else if (!wi.next(w)) {
+                if (dyn && lane == 0) {
+                    if (!ring_get<kCluster>(ctl, ring, ring_full, leader_ring_empty, seq, w))
+                        st = 0;
+                    else if (w.tile < 0)
                         st = 2;
-                    } else if (pingpong) {
-                        WorkItem skip;  // the other group's item
-                        wi.next(skip);
-                    }
                 }
                 st = __shfl_sync(0xFFFFFFFFu, st, 0);
                 if (st == 1u &&
                     !warp_wait<kCluster>(ctl, accf_bar + 8u * acc, acc_ph, kRoleEpilogue, (uint32_t)acc, lane))
                     st = 0;
                 if (lane == 0) {
-                    st_volatile_shared_u32(go + 4u, (uint32_t)w.tile);
-                    st_volatile_shared_u32(go + 8u, (uint32_t)w.kb0);
-                    st_volatile_shared_u32(go + 12u, (uint32_t)w.kb1);
+                    if (dyn) {
+                        st_volatile_shared_u32(go + 4u, (uint32_t)w.tile);
+                        st_volatile_shared_u32(go + 8u, (uint32_t)w.kb0);
+                        st_volatile_shared_u32(go + 12u, (uint32_t)w.kb1);
+                    }
                     st_volatile_shared_u32(go, st);
                 }
             }
             named_barrier_sync(1u + (uint32_t)grp, group_threads);
             if (ld_volatile_shared_u32(go) != 1u)
                 break;
-            WorkItem w;
-            w.tile = (int32_t)ld_volatile_shared_u32(go + 4u);
-            w.kb0 = (int32_t)ld_volatile_shared_u32(go + 8u);
-            w.kb1 = (int32_t)ld_volatile_shared_u32(go + 12u);
+            if (dyn) {
+                w.tile = (int32_t)ld_volatile_shared_u32(go + 4u);
+                w.kb0 = (int32_t)ld_volatile_shared_u32(go + 8u);
+                w.kb1 = (int32_t)ld_volatile_shared_u32(go + 12u);
+                tc = tile_coord(w.tile, p);
+            }
             seq += seq_step;
             tc_fence_after_sync();
-            const TileCoord tc = tile_coord(w.tile, p);
             const int32_t y = tc.mb * kTileM + (int32_t)rank * kBlockM + q * 32;
             // A stream-K item that does not start at k-block 0 is a contributor: it
             // leaves its fp32 partial for the tile's owner.  The item holding
@@ -524,7 +536,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     __syncwarp();
                     if (lane == 0) {
                         if constexpr (kCluster)
-                            mbar_arrive_cluster(acce_target + 8u * acc);
+                            mbar_arrive_cluster_handoff(acce_target + 8u * acc);
                         else
                             mbar_arrive(acce_bar + 8u * acc);
                     }

@@ -116,6 +116,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Arrive on a barrier given by its shared::cluster address (own or peer CTA)
+// with release at CTA scope only.  For hand-offs that publish no memory
+// through the barrier -- tensor memory drained, ordered by the tcgen05 fences
+// around it -- so that the arrive does not first wait for this thread's
+// earlier global stores to become visible to the whole cluster.
+__device__ __forceinline__ void mbar_arrive_cluster_handoff(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 // One potentially blocking probe: true once the phase with parity `parity`
 // has completed.  While the phase is open the thread is suspended in hardware
 // for up to `suspend_ns` (it resumes as soon as the phase completes), so a
