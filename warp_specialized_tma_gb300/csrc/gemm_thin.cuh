@@ -159,8 +159,11 @@ __global__ void __launch_bounds__(kThinThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
-    // Everything above touched only this CTA's shared and tensor memory.
-    grid_dependency_wait();
+    // Everything above touched only this CTA's shared and tensor memory, and so
+    // does the work split below (kernel parameters only): both may overlap the
+    // previous kernel on the stream.  The producer and the epilogue wait for
+    // that kernel before their first global access; the MMA issuer touches
+    // only shared and tensor memory.
 
     WaitCtl ctl;
     ctl.abort_flag = abort_flag;
@@ -178,6 +181,7 @@ __global__ void __launch_bounds__(kThinThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
+        grid_dependency_wait();
         int s = 0;
         uint32_t ph = 0;
         int32_t it = 0;
@@ -256,6 +260,7 @@ __global__ void __launch_bounds__(kThinThreads, 1)
         ctl.wait_drain<false>(done_bar, 0u, 0xFFFu);
     } else if (warp >= 4) {
         // ---------------- epilogue ----------------
+        grid_dependency_wait();
         const int q = warp & 3;  // tensor-memory lane quadrant
         const int32_t row_in_tile = q * 32 + lane;
         int acc = 0;

@@ -129,9 +129,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
     // Everything above touched only this CTA's shared and tensor memory, so it
-    // may overlap the previous kernel on the stream; from here on A, B, D, the
-    // workspace and the tile counter are read or written.
-    grid_dependency_wait();
+    // may overlap the previous kernel on the stream.  The roles that read or
+    // write global memory (A, B, D, the workspace, the tile counter) -- the
+    // producer and the epilogue -- wait for that kernel before their first
+    // access; the MMA issuer touches only shared and tensor memory.
 
     WaitCtl ctl;
     ctl.abort_flag = abort_flag;
@@ -171,9 +172,24 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (dyn)
                 wi.dp = wi.T;  // whole tiles come from the counter, not from the grid stride
             WorkItem w;
+            // The first item of the static schedule and its coordinates depend
+            // only on kernel parameters: they are worked out before the wait for
+            // the previous kernel, so that the first loads issue as soon as its
+            // memory is visible.
+            bool first = !dyn;
+            bool have0 = false;
+            TileCoord tc0 = {0, 0};
+            if (first) {
+                have0 = wi.next(w);
+                if (have0)
+                    tc0 = tile_coord(w.tile, p);
+            }
+            grid_dependency_wait();
             for (;;) {
                 bool have;
-                if (!dyn) {
+                if (first) {
+                    have = have0;
+                } else if (!dyn) {
                     have = wi.next(w);
                 } else if (publisher) {
                     // this cluster's stream-K share first, then whole tiles on demand
@@ -207,7 +223,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 }
                 if (!have)
                     break;
-                const TileCoord tc = tile_coord(w.tile, p);
+                const TileCoord tc = first ? tc0 : tile_coord(w.tile, p);
+                first = false;
                 const int32_t ya = tc.mb * kTileM + (int32_t)rank * kBlockM;
                 const int32_t yb = tc.nb * kBlockN + (int32_t)rank * (int32_t)kBRows;
                 // Alternating k direction: all SM pairs are in the same wave of whole
@@ -371,6 +388,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             setmaxnreg_inc<kConsumerRegs>();
 
         // ---------------- epilogue: tile { TMEM -> bf16 -> D } ----------------
+        grid_dependency_wait();
         // Cooperative: both warpgroups drain every tile, a warp takes 32 rows x
         // 128 columns.  Ping-pong: warpgroup g drains the items that use
         // accumulator g (items g, g+2, ... of the sequence), a warp takes 32 rows
