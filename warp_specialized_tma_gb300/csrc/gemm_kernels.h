@@ -110,6 +110,7 @@ struct ThinParams {
     int32_t stages;
     int32_t transposed;     // 1: the large operand is B, so D[m][n] is accumulator row n, column m
     int32_t d_vec;          // 1: rows of D are 16-byte aligned (vector stores, not transposed only)
+    int32_t d_pair;         // 1: rows of D are 4-byte aligned (paired stores, transposed only)
     int32_t fault_skip_it;  // test hook, -1 = off
     int64_t ldd;
     void *D;

@@ -70,20 +70,43 @@ __device__ __forceinline__ uint16_t thin_bf16(float f)
 
 // Stores one accumulator row (this thread's row r of the large operand's tile)
 // to D.  Not transposed: D[r][0 .. thin).  Transposed: D[0 .. thin)[r], so the
-// 32 lanes of a warp store 32 consecutive elements of one row of D.
+// 32 lanes of a warp store 32 consecutive elements of one row of D; when the
+// warp's 32 columns all lie inside D and its rows are 4-byte aligned, lane
+// pairs trade one value per two rows (the even lane stores row i of columns
+// r, r + 1, the odd lane row i + 1) and store 4-byte words, half as many
+// stores.  Called by all 32 lanes of a warp.
 template <int NT>
 __device__ __forceinline__ void thin_store_row(const float (&v)[NT], int64_t r, const ThinParams &p)
 {
-    if (r >= p.rows)
-        return;
     uint16_t *const D = static_cast<uint16_t *>(p.D);
     if (p.transposed) {
+        const int lane = (int)(threadIdx.x & 31u);
+        if (p.d_pair && !p.fused && r - lane + 32 <= p.rows) {
+            const bool odd = (lane & 1) != 0;
+#pragma unroll
+            for (int i = 0; i < NT; i += 2) {
+                const float got = __shfl_xor_sync(0xFFFFFFFFu, odd ? v[i] : v[i + 1], 1);
+                if (!odd) {
+                    if (i < p.thin)
+                        *reinterpret_cast<uint32_t *>(D + (int64_t)i * p.ldd + r) =
+                            pack_bf16x2(__float_as_uint(v[i]), __float_as_uint(got));
+                } else if (i + 1 < p.thin) {
+                    *reinterpret_cast<uint32_t *>(D + (int64_t)(i + 1) * p.ldd + r - 1) =
+                        pack_bf16x2(__float_as_uint(got), __float_as_uint(v[i + 1]));
+                }
+            }
+            return;
+        }
+        if (r >= p.rows)
+            return;
 #pragma unroll
         for (int i = 0; i < NT; ++i)
             if (i < p.thin)
                 D[(int64_t)i * p.ldd + r] = thin_bf16(thin_epilogue_value(v[i], i, r, p));
         return;
     }
+    if (r >= p.rows)
+        return;
     uint16_t *const row = D + r * p.ldd;
     if (p.d_vec && !p.fused && p.thin == NT) {
 #pragma unroll
@@ -311,12 +334,16 @@ __global__ void __launch_bounds__(kThinThreads, 1)
                 continue;
             }
             // a piece of a split tile: leave the partial, count it, and let the
-            // last piece add every partial in range order and store the tile
-            float *const mine =
-                p.partials + ((size_t)thin_slot(p.units, G, KB, j, t) * kBlockM + (size_t)row_in_tile) * NT;
+            // last piece add every partial in range order and store the tile.
+            // A slot holds the 128 x NT fp32 partial as NT / 4 columns of
+            // float4, each column the 128 rows in order, so that the four
+            // groups of 4 columns a warp stores (or loads) at a time are 512
+            // contiguous bytes each.
+            float4 *const mine = reinterpret_cast<float4 *>(p.partials) +
+                                 (size_t)thin_slot(p.units, G, KB, j, t) * (kBlockM * NT / 4) + row_in_tile;
 #pragma unroll
             for (int i = 0; i < NT; i += 4)
-                *reinterpret_cast<float4 *>(mine + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                __stcg(mine + (i >> 2) * kBlockM, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
             __threadfence();
             named_barrier_sync(1u, 128u);
             const int32_t jf = thin_range_of(p.units, G, t * KB);
@@ -332,11 +359,11 @@ __global__ void __launch_bounds__(kThinThreads, 1)
             for (int i = 0; i < NT; ++i)
                 sum[i] = 0.f;
             for (int32_t jj = jf; jj <= jl; ++jj) {
-                const float *part =
-                    p.partials + ((size_t)thin_slot(p.units, G, KB, jj, t) * kBlockM + (size_t)row_in_tile) * NT;
+                const float4 *part = reinterpret_cast<const float4 *>(p.partials) +
+                                     (size_t)thin_slot(p.units, G, KB, jj, t) * (kBlockM * NT / 4) + row_in_tile;
 #pragma unroll
                 for (int i = 0; i < NT; i += 4) {
-                    const float4 f = __ldcg(reinterpret_cast<const float4 *>(part + i));
+                    const float4 f = __ldcg(part + (i >> 2) * kBlockM);
                     sum[i] += f.x;
                     sum[i + 1] += f.y;
                     sum[i + 2] += f.z;
