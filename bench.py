@@ -617,20 +617,25 @@ def run_ours(args):
         j = i % 2
         gs[j].run_host(hA, hB, hDs[j], *bufs[j], streams[j])
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0.record(streams[0])
-    streams[1].wait_event(e0)
-    for i in range(args.e2e_steps):
-        j = i % 2
-        gs[j].run_host(hA, hB, hDs[j], *bufs[j], streams[j])
-    streams[0].wait_stream(streams[1])
-    e1.record(streams[0])
-    torch.cuda.synchronize(dev)
-    e2e_ms = dist.max(e0.elapsed_time(e1), dev)
-    e2e_value = aggregate(flops, args.e2e_steps, e2e_ms, world)
+    # The host link is shared with whatever else the host does, so the loop is
+    # timed three times and the median is reported (all three are kept).
+    def e2e_loop():
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(streams[0])
+        streams[1].wait_event(e0)
+        for i in range(args.e2e_steps):
+            j = i % 2
+            gs[j].run_host(hA, hB, hDs[j], *bufs[j], streams[j])
+        streams[0].wait_stream(streams[1])
+        e1.record(streams[0])
+        torch.cuda.synchronize(dev)
+        return dist.max(e0.elapsed_time(e1), dev)
+
+    e2e_runs = [aggregate(flops, args.e2e_steps, e2e_loop(), world) for _ in range(3)]
+    e2e_value = statistics.median(e2e_runs)
 
     # Library comparator (not an oracle): cuBLAS through torch.matmul on the
     # same device operands, outside the timed region above.  The GPU's clock
@@ -674,19 +679,23 @@ def run_ours(args):
     for i in range(4):
         copies(i)
     torch.cuda.synchronize(dev)
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize(dev)
-    c0.record(streams[0])
-    streams[1].wait_event(c0)
-    for i in range(args.e2e_steps):
-        copies(i)
-    streams[0].wait_stream(streams[1])
-    c1.record(streams[0])
-    torch.cuda.synchronize(dev)
-    copy_ms = dist.max(c0.elapsed_time(c1), dev)
-    copy_bound = aggregate(flops, args.e2e_steps, copy_ms, world)
+
+    def copy_loop():
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        c0.record(streams[0])
+        streams[1].wait_event(c0)
+        for i in range(args.e2e_steps):
+            copies(i)
+        streams[0].wait_stream(streams[1])
+        c1.record(streams[0])
+        torch.cuda.synchronize(dev)
+        return dist.max(c0.elapsed_time(c1), dev)
+
+    copy_runs = [aggregate(flops, args.e2e_steps, copy_loop(), world) for _ in range(3)]
+    copy_bound = statistics.median(copy_runs)
     for gg in gs:
         st, detail = gg.device_status()
         if st != binding.OK:
@@ -769,7 +778,9 @@ def run_ours(args):
                     "d2h_bytes_per_step": 2 * M * N, "streams": 2,
                     "call": "gemm_bf16_run_host (H2D A,B + GEMM + D2H D per step)",
                     "bound": "host link", "copies_only_value": copy_bound,
-                    "frac_of_copy_bound": e2e_value / copy_bound},
+                    "frac_of_copy_bound": e2e_value / copy_bound,
+                    "runs": e2e_runs, "copies_only_runs": copy_runs,
+                    "note": "median of 3 timed loops of e2e_steps steps each"},
             "detail": {
                 "launch_ms": {"mean": kernel_ms, "median": statistics.median(launch_ms), "best": min(launch_ms)},
                 "tflops_best_launch": flops / (min(launch_ms) * 1e-3) / 1e12,
