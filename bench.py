@@ -617,8 +617,12 @@ def run_ours(args):
         j = i % 2
         gs[j].run_host(hA, hB, hDs[j], *bufs[j], streams[j])
     torch.cuda.synchronize(dev)
-    # The host link is shared with whatever else the host does, so the loop is
-    # timed three times and the median is reported (all three are kept).
+    # Loops of this pattern run in one of two modes on GB300: the two streams'
+    # copies overlap (~1.48 ms per step), or, in about one loop in ten in
+    # isolation and more often right after heavy GEMM load, they serialise
+    # (~2.47 ms per step) -- whatever the copy call (plain torch copies do the
+    # same).  So the loop is timed five times and the median is reported, with
+    # every run kept.
     def e2e_loop():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -634,7 +638,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return dist.max(e0.elapsed_time(e1), dev)
 
-    e2e_runs = [aggregate(flops, args.e2e_steps, e2e_loop(), world) for _ in range(3)]
+    e2e_runs = [aggregate(flops, args.e2e_steps, e2e_loop(), world) for _ in range(5)]
     e2e_value = statistics.median(e2e_runs)
 
     # Library comparator (not an oracle): cuBLAS through torch.matmul on the
@@ -694,7 +698,7 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return dist.max(c0.elapsed_time(c1), dev)
 
-    copy_runs = [aggregate(flops, args.e2e_steps, copy_loop(), world) for _ in range(3)]
+    copy_runs = [aggregate(flops, args.e2e_steps, copy_loop(), world) for _ in range(5)]
     copy_bound = statistics.median(copy_runs)
     for gg in gs:
         st, detail = gg.device_status()
@@ -780,7 +784,7 @@ def run_ours(args):
                     "bound": "host link", "copies_only_value": copy_bound,
                     "frac_of_copy_bound": e2e_value / copy_bound,
                     "runs": e2e_runs, "copies_only_runs": copy_runs,
-                    "note": "median of 3 timed loops of e2e_steps steps each"},
+                    "note": "median of 5 timed loops of e2e_steps steps each"},
             "detail": {
                 "launch_ms": {"mean": kernel_ms, "median": statistics.median(launch_ms), "best": min(launch_ms)},
                 "tflops_best_launch": flops / (min(launch_ms) * 1e-3) / 1e12,

@@ -1113,6 +1113,25 @@ GEMM_BF16_API int gemm_bf16_run_fused(gemm_bf16_t h, const void *A, const void *
     return run_impl(h, A, B, D, &fz, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// `rows` rows of `cols` bf16 between two buffers of row pitch `ld` (elements):
+// one linear copy when the rows are contiguous, else a pitched copy of the
+// sub-matrix (the padding between rows is not copied).
+cudaError_t copy_rows(void *dst, const void *src, int64_t ld, int64_t cols, int64_t rows, cudaMemcpyKind kind,
+                      cudaStream_t st)
+{
+    if (ld == cols)
+        return cudaMemcpyAsync(dst, src, (size_t)(rows * cols * 2), kind, st);
+    return cudaMemcpy2DAsync(dst, (size_t)(ld * 2), src, (size_t)(ld * 2), (size_t)(cols * 2), (size_t)rows, kind, st);
+}
+
+}  // namespace
+
+extern "C" {
+
 GEMM_BF16_API int gemm_bf16_run_host(gemm_bf16_t h, const void *hA, const void *hB, void *hD, void *dA, void *dB,
                                      void *dD, void *stream)
 {
@@ -1125,17 +1144,14 @@ GEMM_BF16_API int gemm_bf16_run_host(gemm_bf16_t h, const void *hA, const void *
     if (rc != GEMM_BF16_OK)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpy2DAsync(dA, pl.lda * 2, hA, pl.lda * 2, pl.K * 2, pl.M, cudaMemcpyHostToDevice, st) !=
-            cudaSuccess ||
-        cudaMemcpy2DAsync(dB, pl.ldb * 2, hB, pl.ldb * 2, pl.K * 2, pl.N, cudaMemcpyHostToDevice, st) !=
-            cudaSuccess) {
+    if (copy_rows(dA, hA, pl.lda, pl.K, pl.M, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        copy_rows(dB, hB, pl.ldb, pl.K, pl.N, cudaMemcpyHostToDevice, st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;
     }
     if ((rc = gemm_bf16_run(h, dA, dB, dD, stream)) != GEMM_BF16_OK)
         return rc;
-    if (cudaMemcpy2DAsync(hD, pl.ldd * 2, dD, pl.ldd * 2, pl.N * 2, pl.M, cudaMemcpyDeviceToHost, st) !=
-        cudaSuccess) {
+    if (copy_rows(hD, dD, pl.ldd, pl.N, pl.M, cudaMemcpyDeviceToHost, st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;
     }
