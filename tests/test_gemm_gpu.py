@@ -862,17 +862,21 @@ def test_tensormap_failure_is_reported_before_launch():
     check(dD.cpu(), A, B, M, N, K, exact=True)
 
 
-def test_run_host_end_to_end():
-    M, N, K = 700, 600, 300
-    A, B = inputs.make_problem(M, N, K, "normal", seed=4, lda=pad8(K), ldb=pad8(K))
+@pytest.mark.parametrize("K,padded_ab,ldd", [(300, True, 600), (296, False, 608), (296, False, 600)])
+def test_run_host_end_to_end(K, padded_ab, ldd):
+    # padded rows take a pitched copy, contiguous rows one linear copy; padding
+    # columns of D are not copied back (the host keeps its sentinel there)
+    M, N = 700, 600
+    ld = pad8(K) + 8 if padded_ab else K
+    A, B = inputs.make_problem(M, N, K, "normal", seed=4, lda=ld, ldb=ld)
     hA, hB = A.pin_memory(), B.pin_memory()
-    hD = torch.zeros((M, N), dtype=torch.bfloat16).pin_memory()
+    hD = torch.full((M, ldd), SENTINEL_BITS, dtype=torch.int16).view(torch.bfloat16).pin_memory()
     dev = torch.device("cuda:0")
     dA = torch.empty_like(A, device=dev)
     dB = torch.empty_like(B, device=dev)
-    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dD = torch.empty((M, ldd), dtype=torch.bfloat16, device=dev)
     with binding.Gemm(0) as g:
-        g.plan(M, N, K, pad8(K), pad8(K), N)
+        g.plan(M, N, K, ld, ld, ldd)
         g.run_host(hA, hB, hD, dA, dB, dD)
         torch.cuda.synchronize()
         assert g.device_status()[0] == binding.OK
