@@ -172,3 +172,24 @@ def test_thin_selection():
         assert g.plan(16, 8192, 8192)["thin"] == 16
     with binding.Gemm(0, thin=0) as g:
         assert g.plan(16, 8192, 8192)["thin"] == 0
+
+
+# The decode-like shapes bench.py reports, at full size and in the default
+# (automatic) launch configuration, every element against the oracle; and the
+# thin kernel at 64 small rows in both orientations.
+@pytest.mark.parametrize("shape,opts", [
+    ((16, 8192, 8192), {}), ((8192, 16, 8192), {}), ((64, 8192, 8192), {}),
+    ((8192, 64, 8192), {}), ((64, 8192, 8192), {"thin": 2}), ((40, 16384, 16384), {"thin": 2}),
+], ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else ",".join(f"{k}={x}" for k, x in v.items()) or "auto")
+def test_skinny_full_size_every_element(shape, opts):
+    from test_gemm_gpu import every_element
+    M, N, K = shape
+    for dist, exact in (("uniform", False), ("int2", True)):
+        A, B = inputs.make_problem(M, N, K, dist, 3 if dist == "uniform" else 103)
+        dev = torch.device("cuda:0")
+        dD = torch.full((M, N), SENTINEL_BITS, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        with binding.Gemm(0, **opts) as g:
+            g.plan(M, N, K)
+            g.run(A.to(dev), B.to(dev), dD)
+            assert g.device_status()[0] == binding.OK
+        every_element(dD.cpu(), A, B, M, N, K, exact=exact)

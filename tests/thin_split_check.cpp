@@ -5,9 +5,10 @@
 // the split; that a tile covered by one range is whole and every other tile's
 // pieces are the ranges from range_of(first unit) to range_of(last unit); that
 // each piece's workspace slot is its range's first- or last-tile slot, and
-// that no two pieces share a slot; and that the epoch-tagged counter counts
-// from zero in each launch, whatever an older launch left in it (for the
-// epochs the host uses: never zero in their low 23 bits).
+// that no two pieces share a slot; and that the owner of each split tile (the
+// piece holding its k-block 0, range_of(t * KB)) is the last tile of its range,
+// so that an owner never waits for anything before its own last item, and the
+// other pieces are not.
 // Prints "ok" and exits 0, or prints the first failure and exits 1.
 #include <cstdio>
 #include <set>
@@ -63,24 +64,15 @@ void check_split(int64_t T, int32_t KB, int32_t G)
             if (whole)
                 continue;
             CHECK(t == b / KB || t == (e - 1) / KB, "tile %lld is inside range %d", (long long)t, j);
+            // the owner holds k-block 0 and is its range's last tile; no other piece holds k-block 0
+            CHECK((kb0 == 0) == (j == jf), "tile %lld piece %d: kb0=%lld but owner %d", (long long)t, j,
+                  (long long)kb0, jf);
+            if (j == jf)
+                CHECK((e - 1) / KB == t, "tile %lld: owner range %d ends in tile %lld", (long long)t, j,
+                      (long long)((e - 1) / KB));
             const int32_t s = thin_slot(U, G, KB, j, t);
             CHECK(s >= 0 && s < 2 * G, "slot %d outside [0, %d)", s, 2 * G);
             CHECK(slots.insert(s).second, "slot %d used twice", s);
-        }
-    }
-}
-
-void check_counter()
-{
-    // the host never launches with an epoch whose low 23 bits are zero
-    for (uint32_t epoch : {1u, 2u, 77u, 0x7FFFFFu, 0x800001u, 0xFFFFFFFFu}) {
-        for (uint32_t left : {0u, 5u, (3u << kThinCountBits) | 2u, ((epoch - 1u) << kThinCountBits) | 3u}) {
-            uint32_t c = left;
-            for (uint32_t k = 1; k <= 20; ++k) {
-                c = thin_count_after(c, epoch);
-                CHECK((c & kThinCountMask) == k, "epoch %u, left %#x: count %u after %u arrivals", epoch, left,
-                      c & kThinCountMask, k);
-            }
         }
     }
 }
@@ -103,7 +95,6 @@ int main()
                 check_split(T, KB, G);
                 ++n;
             }
-    check_counter();
     if (failures) {
         std::printf("%d failure(s)\n", failures);
         return 1;

@@ -91,11 +91,11 @@ struct gemm_bf16 {
     // packed operand copies (A then B), grown on demand by plan
     void *pack = nullptr;
     size_t pack_bytes = 0;
-    // thin kernel's partials and per-tile counters, grown on demand by plan
+    // thin kernel's partials and their flags, grown on demand by plan
     float *thin_ws = nullptr;
     size_t thin_ws_floats = 0;
-    uint32_t *thin_cnt = nullptr;
-    size_t thin_cnt_n = 0;
+    uint32_t *thin_flags = nullptr;
+    size_t thin_flags_n = 0;
 };
 
 namespace {
@@ -514,9 +514,9 @@ int plan_thin(gemm_bf16_t h, Plan &pl)
     pl.sk_tiles = pl.sk_head = pl.sk_pieces = 0;
     pl.sk_units = 0;
     pl.sk_slots = 0;
-    // two partial slots per CTA (thin_split.h) and a counter per tile; counters
-    // start at 0 and carry the launch's epoch, so a fresh allocation is zeroed
-    // and never reset afterwards
+    // two partial slots per CTA (thin_split.h), each with a flag; a flag holds
+    // the epoch of the launch that last completed the slot's partial, so a
+    // fresh allocation is zeroed and never reset afterwards
     const size_t floats = (size_t)2 * (size_t)pl.grid_ctas * kBlockM * (size_t)pl.thin_nt;
     if (floats > h->thin_ws_floats) {
         float *nws = nullptr;
@@ -529,19 +529,20 @@ int plan_thin(gemm_bf16_t h, Plan &pl)
         h->thin_ws = nws;
         h->thin_ws_floats = floats;
     }
-    if ((size_t)pl.tiles > h->thin_cnt_n) {
+    const size_t slots = (size_t)2 * (size_t)pl.grid_ctas;
+    if (slots > h->thin_flags_n) {
         uint32_t *nc = nullptr;
-        if (cudaMalloc(&nc, (size_t)pl.tiles * sizeof(uint32_t)) != cudaSuccess ||
-            cudaMemset(nc, 0, (size_t)pl.tiles * sizeof(uint32_t)) != cudaSuccess) {
+        if (cudaMalloc(&nc, slots * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(nc, 0, slots * sizeof(uint32_t)) != cudaSuccess) {
             cudaGetLastError();
             if (nc)
                 cudaFree(nc);
             return GEMM_BF16_ERR_CUDA;
         }
-        if (h->thin_cnt)
-            cudaFree(h->thin_cnt);
-        h->thin_cnt = nc;
-        h->thin_cnt_n = (size_t)pl.tiles;
+        if (h->thin_flags)
+            cudaFree(h->thin_flags);
+        h->thin_flags = nc;
+        h->thin_flags_n = slots;
     }
     return GEMM_BF16_OK;
 }
@@ -644,8 +645,8 @@ GEMM_BF16_API int gemm_bf16_destroy(gemm_bf16_t h)
         cudaFree(h->pack);
     if (h->thin_ws)
         cudaFree(h->thin_ws);
-    if (h->thin_cnt)
-        cudaFree(h->thin_cnt);
+    if (h->thin_flags)
+        cudaFree(h->thin_flags);
     delete h;
     return GEMM_BF16_OK;
 }
@@ -807,13 +808,12 @@ struct FusedArgs {
     float alpha, beta;
 };
 
-// A launch's epoch: never 0 (the square kernel's flags start at 0) and never 0
-// in the 23 bits the thin kernel's counters keep.
+// A launch's epoch: never 0 (the flags of both kernels start at 0).
 void next_epoch(gemm_bf16_t h)
 {
     do
         ++h->epoch;
-    while ((h->epoch & (0xFFFFFFFFu >> kThinCountBits)) == 0u);
+    while (h->epoch == 0u);
 }
 
 // The operands as run_impl resolved them: the caller's pointers, and the ones
@@ -885,7 +885,7 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
     tp.err = h->d_err;
     tp.watchdog_ns = pl.watchdog_ns;
     tp.partials = h->thin_ws;
-    tp.counters = h->thin_cnt;
+    tp.flags = h->thin_flags;
     next_epoch(h);
     tp.epoch = h->epoch;
     tp.C = nullptr;
@@ -1173,11 +1173,8 @@ GEMM_BF16_API int gemm_bf16_device_status(gemm_bf16_t h, uint32_t *detail)
     // Clearing the whole block also puts the tile counter back to 0: after a
     // watchdog give-up it is the only thing that does (normally the last SM
     // pair of each launch resets it).
-    // After a give-up the thin kernel's tile counters may hold a partial count;
-    // they go back to zero with the status word.
     if (cudaMemcpy(&w, h->d_err, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess ||
         (w != 0 && cudaMemset(h->d_err, 0, 4 * sizeof(uint32_t)) != cudaSuccess) ||
-        (w != 0 && h->thin_cnt && cudaMemset(h->thin_cnt, 0, h->thin_cnt_n * sizeof(uint32_t)) != cudaSuccess) ||
         cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;

@@ -117,7 +117,7 @@ struct ThinParams {
     uint32_t *err;
     uint64_t watchdog_ns;
     float *partials;        // 2 slots per CTA, 128 x NT fp32 each
-    uint32_t *counters;     // one per tile (thin_count_after)
+    uint32_t *flags;        // one per partial slot: == epoch once that partial is complete
     uint32_t epoch;         // this launch's value (never 0)
     // fused epilogue, as in GemmParams
     const void *C;

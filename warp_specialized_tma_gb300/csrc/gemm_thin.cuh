@@ -17,9 +17,10 @@
 //                    "empty"; after an item, commit -> accumulator full
 //   warp 2           allocates (and frees) tensor memory
 //   warps 4-7        epilogue: tensor memory -> registers; whole tiles are
-//                    stored directly, pieces of split tiles leave an fp32
-//                    partial, and the last piece to finish adds the others and
-//                    stores the tile (thin_split.h)
+//                    stored directly; of a split tile's pieces, the one holding
+//                    k-block 0 (the last item of its range) adds the others'
+//                    fp32 partials once their flags are up and stores the tile
+//                    (thin_split.h)
 // Every wait is bounded by the watchdog (WaitCtl in ptx.cuh).
 #pragma once
 
@@ -37,17 +38,21 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu_u32_thin(const uint32_t *p)
     return v;
 }
 
-// Counts this piece of tile t; true when it is the tile's last piece.
-__device__ __forceinline__ bool thin_arrive(uint32_t *counter, uint32_t epoch, uint32_t pieces)
+// Thread 128 waits (bounded) until the flag of a later piece's partial
+// carries this launch's epoch; false if the wait gave up.
+__device__ __forceinline__ bool thin_wait_flag(const WaitCtl &ctl, const uint32_t *flag, uint32_t epoch)
 {
-    uint32_t cur = ld_acquire_gpu_u32_thin(counter);
-    for (;;) {
-        const uint32_t nv = thin_count_after(cur, epoch);
-        const uint32_t prev = atomicCAS(counter, cur, nv);
-        if (prev == cur)
-            return (nv & kThinCountMask) == pieces;
-        cur = prev;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 0; ld_acquire_gpu_u32_thin(flag) != epoch; ++n) {
+        if (ctl.aborted())
+            return false;
+        if ((n & 63u) == 63u && (globaltimer_ns() - t0 > ctl.limit_ns || n > (1u << 30))) {
+            ctl.fail(kRoleFixup, 0);
+            return false;
+        }
+        __nanosleep(64);
     }
+    return true;
 }
 
 // fp32 accumulator element -> the stored value (fused: alpha * acc + beta * C + bias).
@@ -333,48 +338,53 @@ __global__ void __launch_bounds__(kThinThreads, 1)
                 thin_store_row<NT>(v, r, p);  // this range holds the whole tile
                 continue;
             }
-            // a piece of a split tile: leave the partial, count it, and let the
-            // last piece add every partial in range order and store the tile.
-            // A slot holds the 128 x NT fp32 partial as NT / 4 columns of
-            // float4, each column the 128 rows in order, so that the four
-            // groups of 4 columns a warp stores (or loads) at a time are 512
-            // contiguous bytes each.
-            float4 *const mine = reinterpret_cast<float4 *>(p.partials) +
-                                 (size_t)thin_slot(p.units, G, KB, j, t) * (kBlockM * NT / 4) + row_in_tile;
+            // A piece of a split tile.  The piece that holds k-block 0 owns the
+            // tile: it is always the last item of its range, while the other
+            // pieces (the start of a later range, or a whole later range) leave
+            // their fp32 partials in workspace slots and raise the slots' flags
+            // to this launch's epoch.  The owner waits for each flag, adds the
+            // partials to its own sums in range order (a fixed order, so the
+            // result does not depend on which piece finishes first) and stores
+            // the tile.  A slot holds the 128 x NT partial as NT / 4 columns of
+            // float4, each column the 128 rows in order, so that the four groups
+            // of 4 columns a warp stores or loads at a time are 512 contiguous
+            // bytes each.
+            if (kb0 > 0) {
+                const int32_t slot = thin_slot(p.units, G, KB, j, t);
+                float4 *const mine =
+                    reinterpret_cast<float4 *>(p.partials) + (size_t)slot * (kBlockM * NT / 4) + row_in_tile;
 #pragma unroll
-            for (int i = 0; i < NT; i += 4)
-                __stcg(mine + (i >> 2) * kBlockM, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
-            __threadfence();
-            named_barrier_sync(1u, 128u);
-            const int32_t jf = thin_range_of(p.units, G, t * KB);
+                for (int i = 0; i < NT; i += 4)
+                    __stcg(mine + (i >> 2) * kBlockM, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                __threadfence();
+                named_barrier_sync(1u, 128u);
+                if (threadIdx.x == 128)
+                    st_release_gpu_u32(p.flags + slot, p.epoch);
+                continue;
+            }
             const int32_t jl = thin_range_of(p.units, G, (t + 1) * KB - 1);
-            if (threadIdx.x == 128)
-                st_volatile_shared_u32(last_word, thin_arrive(p.counters + t, p.epoch, (uint32_t)(jl - jf + 1)) ? 1u : 0u);
+            if (threadIdx.x == 128) {
+                uint32_t ok = 1u;
+                for (int32_t jj = j + 1; jj <= jl && ok; ++jj)
+                    ok = thin_wait_flag(ctl, p.flags + thin_slot(p.units, G, KB, jj, t), p.epoch) ? 1u : 0u;
+                st_volatile_shared_u32(last_word, ok);
+            }
             named_barrier_sync(1u, 128u);
             if (ld_volatile_shared_u32(last_word) == 0u)
-                continue;
-            __threadfence();
-            float sum[NT];
-#pragma unroll
-            for (int i = 0; i < NT; ++i)
-                sum[i] = 0.f;
-            for (int32_t jj = jf; jj <= jl; ++jj) {
+                break;  // the watchdog gave up
+            for (int32_t jj = j + 1; jj <= jl; ++jj) {
                 const float4 *part = reinterpret_cast<const float4 *>(p.partials) +
                                      (size_t)thin_slot(p.units, G, KB, jj, t) * (kBlockM * NT / 4) + row_in_tile;
 #pragma unroll
                 for (int i = 0; i < NT; i += 4) {
                     const float4 f = __ldcg(part + (i >> 2) * kBlockM);
-                    sum[i] += f.x;
-                    sum[i + 1] += f.y;
-                    sum[i + 2] += f.z;
-                    sum[i + 3] += f.w;
+                    v[i] += f.x;
+                    v[i + 1] += f.y;
+                    v[i + 2] += f.z;
+                    v[i + 3] += f.w;
                 }
             }
-            thin_store_row<NT>(sum, r, p);
-            // the next launch's first piece of this tile starts from zero
-            named_barrier_sync(1u, 128u);
-            if (threadIdx.x == 128)
-                p.counters[t] = 0u;
+            thin_store_row<NT>(v, r, p);
         }
     }
 

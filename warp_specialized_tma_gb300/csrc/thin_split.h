@@ -8,8 +8,8 @@
 // and its last tile may be partial, and so a range leaves at most two fp32
 // partials: slot 2j for its first tile and slot 2j + 1 for its last.  The
 // pieces of tile t are the ranges from range_of(t KB) to range_of((t + 1) KB - 1).
-// The last piece to finish adds the others' partials, in range order, and
-// stores the tile.
+// The piece holding the tile's k-block 0 (the owner, see below) adds the
+// other pieces' partials, in range order, and stores the tile.
 #pragma once
 
 #include <stdint.h>
@@ -41,21 +41,14 @@ WSTMA_THIN_FN int32_t thin_slot(int64_t U, int32_t G, int32_t KB, int32_t j, int
     return 2 * j + (t == thin_begin(U, G, j) / KB ? 0 : 1);
 }
 
-// Tile-completion counter: the launch's epoch in the high 23 bits, the pieces
-// that have arrived in the low 9.  A counter left by an older launch (another
-// epoch) counts as zero.  The host never uses an epoch whose low 23 bits are
-// zero, the last piece of a tile puts its counter back to zero, and after a
-// watchdog give-up the host clears the counters; so a count from a launch
-// 2^23 launches back, which would carry the same epoch bits, is never left.
-constexpr uint32_t kThinCountBits = 9;
-constexpr uint32_t kThinCountMask = (1u << kThinCountBits) - 1u;
-constexpr int32_t kThinMaxGrid = (int32_t)kThinCountMask;
+// The owner of a split tile is the piece that holds its k-block 0, i.e. the
+// range thin_range_of(t * KB).  That piece is always the last item of its
+// range: a range that starts inside the tile ends in a later tile, and one
+// that starts at the tile's first unit without ending at its last one ends
+// inside it.  The other pieces leave partials and raise their slots' flags;
+// the owner adds them in range order.
 
-WSTMA_THIN_FN uint32_t thin_count_after(uint32_t cur, uint32_t epoch)
-{
-    const uint32_t ep = epoch & (0xFFFFFFFFu >> kThinCountBits);
-    const uint32_t have = (cur >> kThinCountBits) == ep ? (cur & kThinCountMask) : 0u;
-    return (ep << kThinCountBits) | (have + 1u);
-}
+// The grid is one CTA per SM; this bounds the partial slots (2 per CTA).
+constexpr int32_t kThinMaxGrid = 1024;
 
 }  // namespace wstma
