@@ -180,10 +180,8 @@ typedef enum gemm_bf16_option {
                                         WATCHDOG_NS, FAULT_SKIP_LOAD, PDL, REPACK and
                                         FAULT_TENSORMAP apply to it.
                                         1 (default) = automatic: the thin kernel where it measured
-                                        faster on GB300 -- min(M, N) <= 16 with max(M, N) >= 4096 and
-                                        K >= 4096; N <= 64 with M >= 8192 and K >= 8192; M <= 64
-                                        with N >= 4096 and K >= 16384 -- and only while every option
-                                        that shapes the
+                                        faster on GB300, min(M, N) <= 64 with max(M, N) >= 4096 and
+                                        K >= 2048, and only while every option that shapes the
                                         square kernel (PIPELINE, CTA_GROUP, PERSISTENT, ACC_BUFFERS,
                                         SETMAXNREG, STAGES, EPILOGUE, MAX_CTAS, STAGE_GROUP,
                                         EPI_SCHEDULE, SCHEDULER) is at its default;

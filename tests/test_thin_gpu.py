@@ -153,14 +153,12 @@ def test_thin_selection():
         assert g.plan(16, 8192, 8192)["thin"] == 16
         assert g.plan(1, 8192, 8192)["thin"] == 16
         assert g.plan(8192, 16, 4096)["thin"] == 16
-        assert g.plan(8192, 17, 8192)["thin"] == 32   # B of 17-64 rows against >= 8192 rows, K >= 8192
-        assert g.plan(16384, 64, 16384)["thin"] == 64
-        assert g.plan(8192, 64, 4096)["thin"] == 0    # ... but not at K < 8192
-        assert g.plan(4096, 64, 8192)["thin"] == 0    # ... nor against < 8192 rows
-        assert g.plan(32, 8192, 8192)["thin"] == 0    # A of 17-64 rows: only at K >= 16384
-        assert g.plan(64, 16384, 16384)["thin"] == 64
-        assert g.plan(16, 4000, 8192)["thin"] == 0  # too little to stream
-        assert g.plan(16, 8192, 4088)["thin"] == 0
+        assert g.plan(8192, 17, 8192)["thin"] == 32   # up to 64 rows, either operand
+        assert g.plan(64, 4096, 2048)["thin"] == 64
+        assert g.plan(4096, 48, 2048)["thin"] == 48
+        assert g.plan(16, 4096, 2040)["thin"] == 0    # K < 2048: the square kernel measured faster
+        assert g.plan(16, 4000, 8192)["thin"] == 0    # too little to stream
+        assert g.plan(65, 8192, 8192)["thin"] == 0
         assert g.plan(8192, 8192, 8192)["thin"] == 0
     with binding.Gemm(0, thin=2) as g:
         assert g.plan(33, 33, 104)["thin"] == 48

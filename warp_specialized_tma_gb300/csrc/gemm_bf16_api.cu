@@ -705,19 +705,11 @@ GEMM_BF16_API int gemm_bf16_plan(gemm_bf16_t h, int64_t M, int64_t N, int64_t K,
         h->opt[GEMM_BF16_OPT_EPILOGUE] == 0 && h->opt[GEMM_BF16_OPT_MAX_CTAS] == 0 &&
         h->opt[GEMM_BF16_OPT_STAGE_GROUP] == 0 && h->opt[GEMM_BF16_OPT_EPI_SCHEDULE] == 0 &&
         h->opt[GEMM_BF16_OPT_SCHEDULER] == 0;
-    // automatic: where the thin kernel measured faster on GB300 --
-    //  - one operand of at most 16 rows streamed against >= 4096 rows of the
-    //    other with K >= 4096 (+2-13 %, +40 % at M = 1);
-    //  - B of at most 64 rows (D's rows are the accumulator's rows) against
-    //    >= 8192 rows of A with K >= 8192 (+2-7 %);
-    //  - A of at most 64 rows (D is stored transposed) with K >= 16384
-    //    (+3-4 %);
-    // with K <= 2048, or 24-64 rows of A at K <= 8192, it was as fast or slower
-    const int64_t small_rows = std::min(M, N), large_rows = std::max(M, N);
-    const bool thin_auto_shape =
-        large_rows >= 4096 && K >= 4096 &&
-        (small_rows <= 16 || (N <= kThinMaxRows && M >= 8192 && K >= 8192) ||
-         (M <= kThinMaxRows && N > kThinMaxRows && K >= 16384));
+    // automatic: where the thin kernel measured faster on GB300, one operand of
+    // at most 64 rows against >= 4096 rows of the other with K >= 2048 (4-25 %
+    // faster in either orientation; even at 64 x 4096 x 4096); at K = 1024 the
+    // square kernel was 20 % faster
+    const bool thin_auto_shape = std::max(M, N) >= 4096 && K >= 2048;
     const bool thin = std::min(M, N) <= kThinMaxRows &&
                       (thin_opt == 2 || (thin_opt == 1 && square_defaults && thin_auto_shape));
     if ((rc = thin ? plan_thin(h, pl) : plan_square(h, pl)) != GEMM_BF16_OK)
