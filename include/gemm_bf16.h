@@ -262,7 +262,7 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
 
 /* Enqueues D = A * B^T on `stream` and returns without synchronising.
  * Launches of one handle share its device scratch (stream-K workspace, tile
- * counter, thin-kernel partials and counters, packed operand copies): do not
+ * counter, thin-kernel partials and flags, packed operand copies): do not
  * let two launches of the same handle run at the same time (e.g. on two
  * streams without an ordering between them);
  * use one handle per stream instead.  When the plan repacks an operand
@@ -273,7 +273,11 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
  * The TMA tensor maps are rebuilt only when a pointer differs from the last run.
  * Argument errors are returned before anything is enqueued; a launch failure
  * returns CUDA.  A watchdog timeout inside the kernel is reported later by
- * gemm_bf16_device_status. */
+ * gemm_bf16_device_status.  The call may be captured into a CUDA graph (plan
+ * outside the capture: planning may allocate).  While `stream` is capturing,
+ * a plan that splits tiles also enqueues a clear of its split-tile flags
+ * before the launch, so that every replay of the graph waits for its own
+ * partial sums. */
 GEMM_BF16_API int gemm_bf16_run(gemm_bf16_t h, const void *A, const void *B, void *D,
                                 void *stream);
 

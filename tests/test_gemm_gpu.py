@@ -705,6 +705,43 @@ def test_cuda_graph_capture_and_replay():
     check(dD.cpu(), (A.float() * -1).to(torch.bfloat16), B, M, N, K, exact=True)
 
 
+@pytest.mark.parametrize("M,N,K,what", [
+    (4096, 4096, 4096, "partial-wave split"),   # 256 tiles: 28 split tiles share flags
+    (1024, 1024, 32768, "head/tail split"),     # 16 tiles, tails on the idle SM pairs
+    (16, 8192, 8192, "thin kernel"),            # split tiles of the thin kernel
+])
+def test_cuda_graph_replays_with_new_inputs(M, N, K, what):
+    # A captured launch keeps the epoch it was captured with; its split tiles'
+    # flags must still mean "written by this replay" on every replay.
+    dev = torch.device("cuda:0")
+    gens = [inputs.make_problem(M, N, K, "int2", seed=60 + i) for i in range(3)]
+    dA = torch.empty_like(gens[0][0], device=dev)
+    dB = torch.empty_like(gens[0][1], device=dev)
+    dD = torch.zeros((M, N), dtype=torch.bfloat16, device=dev)
+    with binding.Gemm(0) as g:
+        info = g.plan(M, N, K)
+        assert info["sk_tiles"] > 0 or info["thin"] > 0, (what, info)
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        dA.copy_(gens[0][0])
+        dB.copy_(gens[0][1])
+        with torch.cuda.stream(s):
+            g.run(dA, dB, dD)          # warm-up outside the capture
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            g.run(dA, dB, dD)
+        for A, B in gens + gens[:1]:
+            dA.copy_(A)
+            dB.copy_(B)
+            dD.zero_()
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            assert g.device_status()[0] == binding.OK
+            check(dD.cpu(), A, B, M, N, K, exact=True)
+
+
 @pytest.mark.parametrize("M,N,K", [(1 << 20, 384, 128), (256, 1 << 19, 64)])
 def test_very_large_m_or_n(M, N, K):
     A, B = inputs.make_problem(M, N, K, "int2", seed=61)

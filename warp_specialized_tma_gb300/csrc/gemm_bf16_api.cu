@@ -817,6 +817,28 @@ struct OperandView {
     void *pack_a, *pack_b;
 };
 
+// Split-tile flags (the square kernel's stream-K slots, the thin kernel's
+// partial slots) mean "written in this launch" when they equal the launch's
+// epoch, a kernel parameter.  A launch captured into a CUDA graph keeps the
+// epoch it was captured with on every replay, so while `st` is capturing, a
+// clear of the flags is enqueued before the launch: each replay then starts
+// from flags no replay has raised yet.  Launches outside a capture need none.
+int clear_flags_if_capturing(uint32_t *flags, size_t n, cudaStream_t st)
+{
+    if (!flags || n == 0)
+        return GEMM_BF16_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    if (cs == cudaStreamCaptureStatusActive && cudaMemsetAsync(flags, 0, n * sizeof(uint32_t), st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_BF16_ERR_CUDA;
+    }
+    return GEMM_BF16_OK;
+}
+
 int launch_repacks(gemm_bf16_t h, const OperandView &ops, cudaStream_t st)
 {
     const Plan &pl = h->plan;
@@ -858,7 +880,8 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
         h->mA = ops.Ae, h->mB = ops.Be, h->mD = nullptr;
         h->maps_valid = true;
     }
-    if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK)
+    if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK ||
+        (rc = clear_flags_if_capturing(h->thin_flags, (size_t)2 * (size_t)pl.grid_ctas, st)) != GEMM_BF16_OK)
         return rc;
 
     ThinParams tp;
@@ -992,6 +1015,8 @@ int run_impl(gemm_bf16_t h, const void *A, const void *B, void *D, const FusedAr
         if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK)
             return rc;
     }
+    if (pl.sk_tiles > 0 && (rc = clear_flags_if_capturing(h->ws_flags, pl.sk_slots, st)) != GEMM_BF16_OK)
+        return rc;
 
     GemmParams prm;
     prm.M = (int32_t)pl.M;
