@@ -705,12 +705,14 @@ def test_cuda_graph_capture_and_replay():
     check(dD.cpu(), (A.float() * -1).to(torch.bfloat16), B, M, N, K, exact=True)
 
 
-@pytest.mark.parametrize("M,N,K,what", [
-    (4096, 4096, 4096, "partial-wave split"),   # 256 tiles: 28 split tiles share flags
-    (1024, 1024, 32768, "head/tail split"),     # 16 tiles, tails on the idle SM pairs
-    (16, 8192, 8192, "thin kernel"),            # split tiles of the thin kernel
+@pytest.mark.parametrize("M,N,K,what,opts", [
+    (4096, 4096, 4096, "partial-wave split", {}),   # 256 tiles: 28 split tiles share flags
+    (1024, 1024, 32768, "head/tail split", {}),     # 16 tiles, tails on the idle SM pairs
+    (16, 8192, 8192, "thin kernel", {}),            # split tiles of the thin kernel
+    (4096, 4096, 4096, "dynamic tile counter", {"scheduler": 1}),
+    (4096, 4096, 4096, "ping-pong epilogue", {"epi_schedule": 1}),
 ])
-def test_cuda_graph_replays_with_new_inputs(M, N, K, what):
+def test_cuda_graph_replays_with_new_inputs(M, N, K, what, opts):
     # A captured launch keeps the epoch it was captured with; its split tiles'
     # flags must still mean "written by this replay" on every replay.
     dev = torch.device("cuda:0")
@@ -718,7 +720,7 @@ def test_cuda_graph_replays_with_new_inputs(M, N, K, what):
     dA = torch.empty_like(gens[0][0], device=dev)
     dB = torch.empty_like(gens[0][1], device=dev)
     dD = torch.zeros((M, N), dtype=torch.bfloat16, device=dev)
-    with binding.Gemm(0) as g:
+    with binding.Gemm(0, **opts) as g:
         info = g.plan(M, N, K)
         assert info["sk_tiles"] > 0 or info["thin"] > 0, (what, info)
         s = torch.cuda.Stream(dev)
