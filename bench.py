@@ -798,7 +798,8 @@ def run_ours(args):
                 "workloads": workloads,
                 "skinny": skinny,
             },
-            "gpu_launches": args.steps,
+            # the GEMM per step, plus the operand copy kernel when the plan repacks
+            "gpu_launches": args.steps * (2 if info["repack"] else 1),
             "clocks": clock_info,
         }
         print(json.dumps(line), flush=True)
