@@ -706,11 +706,11 @@ def test_cuda_graph_capture_and_replay():
 
 
 @pytest.mark.parametrize("M,N,K,what,opts", [
-    (4096, 4096, 4096, "partial-wave split", {}),   # 256 tiles: 28 split tiles share flags
+    (4096, 4096, 1024, "partial-wave split", {}),   # 256 tiles: 28 split tiles share flags
     (1024, 1024, 32768, "head/tail split", {}),     # 16 tiles, tails on the idle SM pairs
     (16, 8192, 8192, "thin kernel", {}),            # split tiles of the thin kernel
-    (4096, 4096, 4096, "dynamic tile counter", {"scheduler": 1}),
-    (4096, 4096, 4096, "ping-pong epilogue", {"epi_schedule": 1}),
+    (4096, 4096, 1024, "dynamic tile counter", {"scheduler": 1}),
+    (4096, 4096, 1024, "ping-pong epilogue", {"epi_schedule": 1}),
 ])
 def test_cuda_graph_replays_with_new_inputs(M, N, K, what, opts):
     # A captured launch keeps the epoch it was captured with; its split tiles'
