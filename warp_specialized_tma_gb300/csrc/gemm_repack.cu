@@ -73,6 +73,10 @@ __global__ void __launch_bounds__(kRepackThreads) repack_rows_kernel(const JobAr
             dst[(int64_t)rr * j.ld_dst + c] = src[(int64_t)rr * j.ld_src + c];
         }
     }
+    // This CTA's rows are copied: the GEMM launched next on the stream (with
+    // programmatic dependent launch) may start its prologue once every CTA of
+    // this grid got here; its loads still wait for this grid's memory.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 JobArgs make_job(const RepackJob &in, int num_sms, int njobs)
