@@ -176,7 +176,7 @@ typedef enum gemm_bf16_option {
                                         (tile, k-block) units split evenly over the SMs, and split
                                         tiles summed in a fixed order from fp32 partials in a
                                         handle-owned workspace (2 slots of 128 x 64 fp32 per SM,
-                                        plus one flag per slot).  Of the other options only
+                                        4 flags per slot, and two words).  Of the other options only
                                         WATCHDOG_NS, FAULT_SKIP_LOAD, PDL, REPACK and
                                         FAULT_TENSORMAP apply to it.
                                         1 (default) = automatic: the thin kernel where it measured

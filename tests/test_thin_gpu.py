@@ -116,7 +116,7 @@ def test_thin_fused_in_place_random_values():
 
 def test_thin_repeated_launches_with_split_tiles():
     # 64 tiles of 128 k-blocks over the SMs: tiles are split, so every launch
-    # counts pieces with a new epoch and the last piece sums the partials
+    # tags its partials with a new epoch and each tile's owner adds them
     M, N, K = 16, 8192, 8192
     dev = torch.device("cuda:0")
     dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -128,6 +128,26 @@ def test_thin_repeated_launches_with_split_tiles():
             g.run(A.to(dev), B.to(dev), dD)
             assert g.device_status()[0] == binding.OK
             check(dD.cpu(), A, B, M, N, K, exact=True)
+
+
+def test_thin_plans_of_other_grids_and_a_fresh_handle_on_freed_memory():
+    # The epoch and the count of CTAs that read it live on the device: plans
+    # with other grid sizes (152 CTAs, then 64 for 8 tiles of 8 k-blocks) must
+    # keep them consistent, and a new handle, whose workspace may reuse the
+    # freed memory of an old one with higher epochs, must start clean.
+    dev = torch.device("cuda:0")
+    shapes = [(16, 8192, 8192), (16, 1024, 512), (8192, 24, 4096), (16, 8192, 8192)]
+    for rounds in range(2):
+        with binding.Gemm(0, thin=2) as g:
+            for i, (M, N, K) in enumerate(shapes):
+                info = g.plan(M, N, K)
+                assert info["thin"] > 0
+                for rep in range(2 + 3 * rounds):
+                    A, B = inputs.make_problem(M, N, K, "int2", seed=200 + 10 * i + rep)
+                    dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                    g.run(A.to(dev), B.to(dev), dD)
+                    assert g.device_status()[0] == binding.OK
+                    check(dD.cpu(), A, B, M, N, K, exact=True)
 
 
 def test_thin_watchdog_gives_up_and_the_handle_recovers():

@@ -91,11 +91,13 @@ struct gemm_bf16 {
     // packed operand copies (A then B), grown on demand by plan
     void *pack = nullptr;
     size_t pack_bytes = 0;
-    // thin kernel's partials and their flags, grown on demand by plan
+    // thin kernel's partials and their flags (grown on demand by plan) and
+    // its device-side epoch and arrival count (allocated once)
     float *thin_ws = nullptr;
     size_t thin_ws_floats = 0;
     uint32_t *thin_flags = nullptr;
     size_t thin_flags_n = 0;
+    uint32_t *thin_sync = nullptr;
 };
 
 namespace {
@@ -514,9 +516,10 @@ int plan_thin(gemm_bf16_t h, Plan &pl)
     pl.sk_tiles = pl.sk_head = pl.sk_pieces = 0;
     pl.sk_units = 0;
     pl.sk_slots = 0;
-    // two partial slots per CTA (thin_split.h), each with a flag; a flag holds
-    // the epoch of the launch that last completed the slot's partial, so a
-    // fresh allocation is zeroed and never reset afterwards
+    // two partial slots per CTA (thin_split.h) of 128 x thin_nt fp32, and a
+    // flag per slot and epilogue warp; a flag holds the epoch of the launch
+    // that last stored that warp's rows, and the epoch starts at 1 and only
+    // grows, so a fresh flag allocation is zeroed and never cleared afterwards
     const size_t floats = (size_t)2 * (size_t)pl.grid_ctas * kBlockM * (size_t)pl.thin_nt;
     if (floats > h->thin_ws_floats) {
         float *nws = nullptr;
@@ -529,20 +532,32 @@ int plan_thin(gemm_bf16_t h, Plan &pl)
         h->thin_ws = nws;
         h->thin_ws_floats = floats;
     }
-    const size_t slots = (size_t)2 * (size_t)pl.grid_ctas;
-    if (slots > h->thin_flags_n) {
-        uint32_t *nc = nullptr;
-        if (cudaMalloc(&nc, slots * sizeof(uint32_t)) != cudaSuccess ||
-            cudaMemset(nc, 0, slots * sizeof(uint32_t)) != cudaSuccess) {
+    const size_t nflags = (size_t)2 * 4 * (size_t)pl.grid_ctas;
+    if (nflags > h->thin_flags_n) {
+        uint32_t *nf = nullptr;
+        if (cudaMalloc(&nf, nflags * sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(nf, 0, nflags * sizeof(uint32_t)) != cudaSuccess) {
             cudaGetLastError();
-            if (nc)
-                cudaFree(nc);
+            if (nf)
+                cudaFree(nf);
             return GEMM_BF16_ERR_CUDA;
         }
         if (h->thin_flags)
             cudaFree(h->thin_flags);
-        h->thin_flags = nc;
-        h->thin_flags_n = slots;
+        h->thin_flags = nf;
+        h->thin_flags_n = nflags;
+    }
+    if (!h->thin_sync) {
+        const uint32_t init[2] = {1u, 0u};  // epoch 1, no CTA arrived
+        uint32_t *ns = nullptr;
+        if (cudaMalloc(&ns, sizeof(init)) != cudaSuccess ||
+            cudaMemcpy(ns, init, sizeof(init), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            if (ns)
+                cudaFree(ns);
+            return GEMM_BF16_ERR_CUDA;
+        }
+        h->thin_sync = ns;
     }
     return GEMM_BF16_OK;
 }
@@ -647,6 +662,8 @@ GEMM_BF16_API int gemm_bf16_destroy(gemm_bf16_t h)
         cudaFree(h->thin_ws);
     if (h->thin_flags)
         cudaFree(h->thin_flags);
+    if (h->thin_sync)
+        cudaFree(h->thin_sync);
     delete h;
     return GEMM_BF16_OK;
 }
@@ -800,7 +817,7 @@ struct FusedArgs {
     float alpha, beta;
 };
 
-// A launch's epoch: never 0 (the flags of both kernels start at 0).
+// A launch's epoch for the square kernel's stream-K flags: never 0 (flags start at 0).
 void next_epoch(gemm_bf16_t h)
 {
     do
@@ -817,9 +834,9 @@ struct OperandView {
     void *pack_a, *pack_b;
 };
 
-// Split-tile flags (the square kernel's stream-K slots, the thin kernel's
-// partial slots) mean "written in this launch" when they equal the launch's
-// epoch, a kernel parameter.  A launch captured into a CUDA graph keeps the
+// The square kernel's stream-K flags mean "written in this launch" when they
+// equal the launch's epoch, a kernel parameter (the thin kernel keeps its
+// epoch in device memory and needs none of this).  A launch captured into a CUDA graph keeps the
 // epoch it was captured with on every replay, so while `st` is capturing, a
 // clear of the flags is enqueued before the launch: each replay then starts
 // from flags no replay has raised yet.  Launches outside a capture need none.
@@ -880,8 +897,7 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
         h->mA = ops.Ae, h->mB = ops.Be, h->mD = nullptr;
         h->maps_valid = true;
     }
-    if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK ||
-        (rc = clear_flags_if_capturing(h->thin_flags, (size_t)2 * (size_t)pl.grid_ctas, st)) != GEMM_BF16_OK)
+    if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK)
         return rc;
 
     ThinParams tp;
@@ -901,8 +917,7 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
     tp.watchdog_ns = pl.watchdog_ns;
     tp.partials = h->thin_ws;
     tp.flags = h->thin_flags;
-    next_epoch(h);
-    tp.epoch = h->epoch;
+    tp.sync = h->thin_sync;
     tp.C = nullptr;
     tp.bias = nullptr;
     tp.ldc = 0;

@@ -117,8 +117,8 @@ struct ThinParams {
     uint32_t *err;
     uint64_t watchdog_ns;
     float *partials;        // 2 slots per CTA, 128 x NT fp32 each
-    uint32_t *flags;        // one per partial slot: == epoch once that partial is complete
-    uint32_t epoch;         // this launch's value (never 0)
+    uint32_t *flags;        // 4 per slot (one per epilogue warp): == epoch once that warp's rows are stored
+    uint32_t *sync;         // {epoch (never 0), CTAs that have read it}, advanced on the device
     // fused epilogue, as in GemmParams
     const void *C;
     const void *bias;

@@ -19,9 +19,19 @@
 //   warps 4-7        epilogue: tensor memory -> registers; whole tiles are
 //                    stored directly; of a split tile's pieces, the one holding
 //                    k-block 0 (the last item of its range) adds the others'
-//                    fp32 partials once their flags are up and stores the tile
-//                    (thin_split.h)
+//                    fp32 partials and stores the tile (thin_split.h)
 // Every wait is bounded by the watchdog (WaitCtl in ptx.cuh).
+//
+// A split tile's pieces meet through fp32 partials in a workspace and one flag
+// per partial slot and epilogue warp.  A contributor warp stores its 32 rows,
+// meets at a warp barrier, and its lane 0 writes the launch's epoch to the
+// flag with a release store; the owner warp's lane 0 polls the flag with
+// acquire loads, the warp meets at a warp barrier, and the 32 lanes read the
+// rows.  The four warps of a CTA do not wait for one another on this path.
+// The epoch lives in device memory: every CTA reads it
+// after the grid-dependency wait, and the last CTA to have read it advances it
+// for the next launch, so launches replayed from a CUDA graph get a new epoch
+// each time as well, and flags never need clearing.
 #pragma once
 
 #include "gemm_kernels.h"
@@ -31,28 +41,28 @@
 
 namespace wstma {
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu_u32_thin(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Thread 128 waits (bounded) until the flag of a later piece's partial
+// Lane 0 of an owner warp waits (bounded) until a contributor warp's flag
 // carries this launch's epoch; false if the wait gave up.
-__device__ __forceinline__ bool thin_wait_flag(const WaitCtl &ctl, const uint32_t *flag, uint32_t epoch)
+__device__ __forceinline__ bool thin_poll_flag(const WaitCtl &ctl, const uint32_t *flag, uint32_t epoch)
 {
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 0; ld_acquire_gpu_u32_thin(flag) != epoch; ++n) {
+    for (uint32_t n = 0; ld_acquire_gpu_u32(flag) != epoch; ++n) {
         if (ctl.aborted())
             return false;
-        if ((n & 63u) == 63u && (globaltimer_ns() - t0 > ctl.limit_ns || n > (1u << 30))) {
+        if (globaltimer_ns() - t0 > ctl.limit_ns || n > (1u << 30)) {
             ctl.fail(kRoleFixup, 0);
             return false;
         }
-        __nanosleep(64);
+        __nanosleep(32);
     }
     return true;
+}
+
+__device__ __forceinline__ uint32_t thin_ld_relaxed_u32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // fp32 accumulator element -> the stored value (fused: alpha * acc + beta * C + bias).
@@ -155,8 +165,8 @@ __global__ void __launch_bounds__(kThinThreads, 1)
     const uint32_t done_bar = acce_bar + 16u;
     const uint32_t tmem_slot = done_bar + 8u;
     const uint32_t abort_flag = tmem_slot + 4u;
-    const uint32_t last_word = abort_flag + 4u;
-    const uint32_t go_words = last_word + 4u;  // 2 words, alternating by item
+    const uint32_t epoch_word = abort_flag + 4u;
+    const uint32_t go_words = epoch_word + 4u;  // 2 words, alternating by item
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -289,6 +299,21 @@ __global__ void __launch_bounds__(kThinThreads, 1)
     } else if (warp >= 4) {
         // ---------------- epilogue ----------------
         grid_dependency_wait();
+        if (threadIdx.x == 128) {
+            // this launch's epoch; the last CTA to read it advances it (the
+            // acquire-release add orders every CTA's read before that store)
+            const uint32_t ep = thin_ld_relaxed_u32(p.sync);
+            st_volatile_shared_u32(epoch_word, ep);
+            uint32_t before;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(before) : "l"(p.sync + 1) : "memory");
+            if (before == (uint32_t)G - 1u) {
+                const uint32_t next = ep + 1u == 0u ? 1u : ep + 1u;
+                asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.sync + 1) : "memory");
+                asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.sync), "r"(next) : "memory");
+            }
+        }
+        named_barrier_sync(1u, 128u);
+        const uint32_t epoch = ld_volatile_shared_u32(epoch_word);
         const int q = warp & 3;  // tensor-memory lane quadrant
         const int32_t row_in_tile = q * 32 + lane;
         int acc = 0;
@@ -341,14 +366,14 @@ __global__ void __launch_bounds__(kThinThreads, 1)
             // A piece of a split tile.  The piece that holds k-block 0 owns the
             // tile: it is always the last item of its range, while the other
             // pieces (the start of a later range, or a whole later range) leave
-            // their fp32 partials in workspace slots and raise the slots' flags
-            // to this launch's epoch.  The owner waits for each flag, adds the
-            // partials to its own sums in range order (a fixed order, so the
-            // result does not depend on which piece finishes first) and stores
-            // the tile.  A slot holds the 128 x NT partial as NT / 4 columns of
-            // float4, each column the 128 rows in order, so that the four groups
-            // of 4 columns a warp stores or loads at a time are 512 contiguous
-            // bytes each.
+            // their fp32 partials in workspace slots and raise one flag per
+            // warp to this launch's epoch.  Each owner warp waits for the flag
+            // of the same warp of every later piece, adds those partials to its
+            // own sums in range order (a fixed order, so the result does not
+            // depend on which piece finishes first) and stores its 32 rows.  A
+            // slot holds the 128 x NT partial as NT / 4 columns of float4, each
+            // column the 128 rows in order, so that a warp's 32 rows of one
+            // column are 512 contiguous bytes.
             if (kb0 > 0) {
                 const int32_t slot = thin_slot(p.units, G, KB, j, t);
                 float4 *const mine =
@@ -356,25 +381,22 @@ __global__ void __launch_bounds__(kThinThreads, 1)
 #pragma unroll
                 for (int i = 0; i < NT; i += 4)
                     __stcg(mine + (i >> 2) * kBlockM, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
-                __threadfence();
-                named_barrier_sync(1u, 128u);
-                if (threadIdx.x == 128)
-                    st_release_gpu_u32(p.flags + slot, p.epoch);
+                __syncwarp();  // the warp's stores come before lane 0's release
+                if (lane == 0)
+                    st_release_gpu_u32(p.flags + (size_t)slot * 4 + q, epoch);
                 continue;
             }
             const int32_t jl = thin_range_of(p.units, G, (t + 1) * KB - 1);
-            if (threadIdx.x == 128) {
-                uint32_t ok = 1u;
-                for (int32_t jj = j + 1; jj <= jl && ok; ++jj)
-                    ok = thin_wait_flag(ctl, p.flags + thin_slot(p.units, G, KB, jj, t), p.epoch) ? 1u : 0u;
-                st_volatile_shared_u32(last_word, ok);
-            }
-            named_barrier_sync(1u, 128u);
-            if (ld_volatile_shared_u32(last_word) == 0u)
-                break;  // the watchdog gave up
             for (int32_t jj = j + 1; jj <= jl; ++jj) {
-                const float4 *part = reinterpret_cast<const float4 *>(p.partials) +
-                                     (size_t)thin_slot(p.units, G, KB, jj, t) * (kBlockM * NT / 4) + row_in_tile;
+                const int32_t sj = thin_slot(p.units, G, KB, jj, t);
+                uint32_t ok = 1u;
+                if (lane == 0)
+                    ok = thin_poll_flag(ctl, p.flags + (size_t)sj * 4 + q, epoch) ? 1u : 0u;
+                __syncwarp();  // lane 0's acquire comes before the lanes' loads
+                if (__shfl_sync(0xFFFFFFFFu, ok, 0) == 0u)
+                    break;  // the watchdog gave up: the rows are stored unsummed, the status says so
+                const float4 *part =
+                    reinterpret_cast<const float4 *>(p.partials) + (size_t)sj * (kBlockM * NT / 4) + row_in_tile;
 #pragma unroll
                 for (int i = 0; i < NT; i += 4) {
                     const float4 f = __ldcg(part + (i >> 2) * kBlockM);
