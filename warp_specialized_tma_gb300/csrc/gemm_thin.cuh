@@ -28,10 +28,10 @@
 // flag with a release store; the owner warp's lane 0 polls the flag with
 // acquire loads, the warp meets at a warp barrier, and the 32 lanes read the
 // rows.  The four warps of a CTA do not wait for one another on this path.
-// The epoch lives in device memory: every CTA reads it
-// after the grid-dependency wait, and the last CTA to have read it advances it
-// for the next launch, so launches replayed from a CUDA graph get a new epoch
-// each time as well, and flags never need clearing.
+// The epoch lives in device memory: every CTA reads it after the
+// grid-dependency wait, and the last CTA to have read it advances it for the
+// next launch, so launches replayed from a CUDA graph get a new epoch each
+// time as well, and flags never need clearing.
 #pragma once
 
 #include "gemm_kernels.h"
