@@ -168,7 +168,7 @@ typedef enum gemm_bf16_option {
                                         encode as a driver error would, and returns
                                         GEMM_BF16_ERR_TENSORMAP before launching anything;
                                         0 (default) = off */
-    GEMM_BF16_OPT_THIN = 21           /* Problems with min(M, N) <= 64 (decode-like, bound by
+    GEMM_BF16_OPT_THIN = 21,          /* Problems with min(M, N) <= 64 (decode-like, bound by
                                         streaming the other operand from HBM) can run on the thin
                                         kernel: the large operand in 128-row tiles is the MMA's M
                                         side, the small one its N side (rounded up to 16, 32, 48 or
@@ -187,6 +187,23 @@ typedef enum gemm_bf16_option {
                                         EPI_SCHEDULE, SCHEDULER) is at its default;
                                         2 = the thin kernel whenever min(M, N) <= 64;
                                         0 = never */
+    GEMM_BF16_OPT_THIN_CLUSTER = 22   /* How the thin kernel splits its work.  Across the SMs: the
+                                        (tile, k-block) units in one contiguous range per SM, split
+                                        tiles summed through the workspace.  Or one tile per
+                                        thread-block cluster of C CTAs: the CTAs split the tile's
+                                        k-blocks, and rank 0 adds the others' fp32 partials, read
+                                        from their shared memory, in rank order (C = 1: one CTA per
+                                        whole tile, nothing to add).  Both orders are fixed, so
+                                        results do not depend on timing.
+                                        1 (default) = automatic: clusters of the largest C <= 8 with
+                                        tiles * C <= SMs whose clusters are all resident at once,
+                                        when tiles * C reaches 60 % of the SMs and each CTA streams
+                                        at most 160 k-blocks (short decode-like problems, where the
+                                        split tiles' traffic through global memory cost more than
+                                        the idle SMs); else across the SMs;
+                                        2..8 = clusters of this size (at most the k-blocks),
+                                        UNSUPPORTED if none can be resident;
+                                        0 = always across the SMs */
 } gemm_bf16_option;
 
 /* What a plan resolved to (filled by gemm_bf16_plan_info). */
@@ -222,6 +239,8 @@ typedef struct gemm_bf16_plan_info_s {
     int32_t thin;                 /* the thin kernel's small-operand width (16, 32, 48 or 64); 0 = the
                                      square kernel.  Then tile_m = 128 rows of the large operand,
                                      tile_n = thin, and tiles counts the large operand's tiles */
+    int32_t thin_cluster;         /* thin kernel: 0 = units split across the SMs; else CTAs per tile
+                                     (1 = whole tiles, >= 2 = a cluster; GEMM_BF16_OPT_THIN_CLUSTER) */
 } gemm_bf16_plan_info_t;
 
 /* Creates a handle bound to CUDA device `device` (-1 = the calling thread's

@@ -65,14 +65,45 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("split", ["sms", "auto"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_thin_exact_integers(shape):
+def test_thin_exact_integers(shape, split):
+    # "sms": the units split across the SMs, split tiles summed through global
+    # memory; "auto": the planner's choice, clusters for most of these shapes
     M, N, K = shape
     ld = (K + 7) // 8 * 8  # rows 16-byte aligned, as TMA needs
     A, B = inputs.make_problem(M, N, K, "int2", seed=M * 7 + N * 3 + K, lda=ld, ldb=ld)
-    D, info = run_thin(A, B, M, N, K)
+    D, info = run_thin(A, B, M, N, K, **({"thin_cluster": 0} if split == "sms" else {}))
     assert info["thin"] == nt_of(M, N) and info["cta_group"] == 1 and info["tile_m"] == 128
+    if split == "sms":
+        assert info["thin_cluster"] == 0
     check(D, A, B, M, N, K, exact=True)
+
+
+# Clusters of C CTAs per tile, every C the option allows (clamped to the
+# k-blocks), on ragged rows and k tails in both orientations: rank 0 adds the
+# others' partials read through distributed shared memory.
+@pytest.mark.parametrize("C", [2, 3, 5, 8])
+@pytest.mark.parametrize("shape", [(16, 1000, 1000), (1000, 40, 700), (48, 2048, 4104), (300, 64, 200), (7, 129, 70)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_thin_cluster_sizes_exact(shape, C):
+    M, N, K = shape
+    ld = (K + 7) // 8 * 8
+    A, B = inputs.make_problem(M, N, K, "int2", seed=C * 1000 + M + N + K, lda=ld, ldb=ld)
+    D, info = run_thin(A, B, M, N, K, thin_cluster=C)
+    KB = (K + 63) // 64
+    assert info["thin_cluster"] == min(C, KB)
+    assert info["grid_ctas"] == info["tiles"] * info["thin_cluster"]
+    check(D, A, B, M, N, K, exact=True)
+
+
+@pytest.mark.parametrize("C", [2, 4])
+def test_thin_cluster_random_values_padded(C):
+    M, N, K = 33, 777, 520
+    A, B = inputs.make_problem(M, N, K, "normal", seed=93, lda=528, ldb=520)
+    D, info = run_thin(A, B, M, N, K, ldd=780, thin_cluster=C)
+    assert info["thin_cluster"] == C
+    check(D, A, B, M, N, K)  # also checks the padding columns of D keep the sentinel
 
 
 @pytest.mark.parametrize("shape,pads", [((2048, 16, 1000), (1008, 1024, 24)), ((16, 2048, 1000), (1016, 1000, 2056)),
@@ -89,13 +120,14 @@ def test_thin_random_values_padded(shape, pads):
 
 @pytest.mark.parametrize("shape", [(2048, 16, 1000), (16, 2048, 1000), (300, 40, 200), (40, 300, 200)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_thin_fused_exact_integers(shape):
+@pytest.mark.parametrize("cluster", [0, 3])
+def test_thin_fused_exact_integers(shape, cluster):
     M, N, K = shape
     A, B = inputs.make_problem(M, N, K, "int2", seed=81)
     g = torch.Generator().manual_seed(82)
     C = inputs.make_operand(M, N, None, "int2", g)
     bias = inputs.make_operand(1, N, None, "int2", g).reshape(-1)
-    D = run_fused_gpu(A, B, M, N, K, C=C, bias=bias, alpha=2.0, beta=-3.0, thin=2)
+    D = run_fused_gpu(A, B, M, N, K, C=C, bias=bias, alpha=2.0, beta=-3.0, thin=2, thin_cluster=cluster)
     _, refbf = oracle.gemm_fused_rows(inputs.bits(A), inputs.bits(B), 2.0, -3.0, C=inputs.bits(C),
                                       bias=inputs.bits(bias))
     assert np.array_equal(inputs.bits(D), refbf)
@@ -114,15 +146,18 @@ def test_thin_fused_in_place_random_values():
     assert np.all(np.abs(D.double().numpy() - ref64) <= tol)
 
 
-def test_thin_repeated_launches_with_split_tiles():
-    # 64 tiles of 128 k-blocks over the SMs: tiles are split, so every launch
-    # tags its partials with a new epoch and each tile's owner adds them
+@pytest.mark.parametrize("cluster", [0, 1])
+def test_thin_repeated_launches_with_split_tiles(cluster):
+    # 64 tiles of 128 k-blocks, split across the SMs (every launch raises its
+    # flags with a new epoch and each tile's owner adds the partials) or in
+    # clusters of 2 (the automatic choice here)
     M, N, K = 16, 8192, 8192
     dev = torch.device("cuda:0")
     dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    with binding.Gemm(0, thin=2) as g:
+    with binding.Gemm(0, thin=2, thin_cluster=cluster) as g:
         info = g.plan(M, N, K)
         assert info["thin"] == 16 and info["tiles"] == 64 and info["grid_ctas"] > info["tiles"]
+        assert info["thin_cluster"] == (0 if cluster == 0 else 2)
         for seed in (101, 102, 103):
             A, B = inputs.make_problem(M, N, K, "int2", seed=seed)
             g.run(A.to(dev), B.to(dev), dD)
@@ -150,13 +185,14 @@ def test_thin_plans_of_other_grids_and_a_fresh_handle_on_freed_memory():
                     check(dD.cpu(), A, B, M, N, K, exact=True)
 
 
-def test_thin_watchdog_gives_up_and_the_handle_recovers():
+@pytest.mark.parametrize("cluster", [0, 4])
+def test_thin_watchdog_gives_up_and_the_handle_recovers(cluster):
     M, N, K = 16, 4096, 4096
     A, B = inputs.make_problem(M, N, K, "int2", seed=111)
     dev = torch.device("cuda:0")
     dA, dB = A.to(dev), B.to(dev)
     dD = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    with binding.Gemm(0, thin=2, watchdog_ns=20_000_000, fault_skip_load=3) as g:
+    with binding.Gemm(0, thin=2, thin_cluster=cluster, watchdog_ns=20_000_000, fault_skip_load=3) as g:
         g.plan(M, N, K)
         g.run(dA, dB, dD)
         st, detail = g.device_status()
@@ -190,6 +226,30 @@ def test_thin_selection():
         assert g.plan(16, 8192, 8192)["thin"] == 16
     with binding.Gemm(0, thin=0) as g:
         assert g.plan(16, 8192, 8192)["thin"] == 0
+
+
+def test_thin_cluster_selection():
+    # automatic: clusters where tiles x C reaches 60 % of the SMs and each CTA
+    # streams at most 160 k-blocks; else the units split across the SMs
+    with binding.Gemm(0) as g:
+        sms = g.plan(16, 8192, 8192)["num_sms"]
+        assert sms == 152  # the figures below are for GB300
+        assert g.plan(16, 8192, 8192)["thin_cluster"] == 2       # 64 tiles
+        assert g.plan(8192, 16, 8192)["thin_cluster"] == 2
+        assert g.plan(64, 8192, 8192)["thin_cluster"] == 2
+        assert g.plan(16, 4096, 8192)["thin_cluster"] == 4       # 32 tiles
+        assert g.plan(16, 12288, 8192)["thin_cluster"] == 1      # 96 whole tiles
+        assert g.plan(16, 16384, 16384)["thin_cluster"] == 0     # 256 k-blocks per CTA: across the SMs
+        assert g.plan(16, 28672, 8192)["thin_cluster"] == 0      # more tiles than SMs
+        assert g.plan(16, 4096, 2048)["thin_cluster"] == 4
+        info = g.plan(16, 8192, 8192)
+        assert info["grid_ctas"] == 128
+    with binding.Gemm(0, thin_cluster=0) as g:
+        assert g.plan(16, 8192, 8192)["thin_cluster"] == 0
+        assert g.plan(16, 8192, 8192)["grid_ctas"] == 152
+    with binding.Gemm(0, thin_cluster=8) as g:
+        info = g.plan(16, 4096, 8192)
+        assert info["thin_cluster"] == 8 and info["grid_ctas"] == 256  # two waves of clusters
 
 
 # The decode-like shapes bench.py reports, at full size and in the default

@@ -53,6 +53,7 @@ OPTIONS = {
     "serpentine": 19,
     "fault_tensormap": 20,
     "thin": 21,
+    "thin_cluster": 22,
 }
 
 # the C entry points and their signatures
@@ -108,6 +109,7 @@ class PlanInfo(ctypes.Structure):
         ("sk_head", ctypes.c_int32),
         ("sk_slots", ctypes.c_int32),
         ("thin", ctypes.c_int32),
+        ("thin_cluster", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

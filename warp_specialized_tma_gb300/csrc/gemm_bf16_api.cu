@@ -23,7 +23,7 @@ using namespace wstma;
 
 namespace {
 
-constexpr int kNumOptions = 22;
+constexpr int kNumOptions = 23;
 constexpr int64_t kMaxDim = 0x7FFFFFFFLL;
 constexpr uint64_t kWatchdogNsPerKBlock = 2000;  // lower bound of the watchdog limit per k-block of K
 
@@ -53,6 +53,8 @@ struct Plan {
     int thin_nt = 0;                          // > 0: the thin kernel, small-operand width 16..64
     bool thin_transposed = false;             // thin kernel: the large operand is B
     int64_t thin_units = 0;                   // thin kernel: tiles * k-blocks
+    int thin_cluster = 0;                     // thin kernel: 0 = units split across the SMs, else
+                                              // CTAs per tile (1 = whole tiles, > 1 = a cluster)
     int64_t tiles = 0;
     int num_m_blocks = 0, num_n_blocks = 0, num_k_blocks = 0;
     int grid_ctas = 0;
@@ -126,6 +128,7 @@ int64_t default_option(int key)
     case GEMM_BF16_OPT_SERPENTINE: return 1;
     case GEMM_BF16_OPT_FAULT_TENSORMAP: return 0;
     case GEMM_BF16_OPT_THIN: return 1;
+    case GEMM_BF16_OPT_THIN_CLUSTER: return 1;
     default: return 0;
     }
 }
@@ -154,6 +157,7 @@ bool option_in_range(int key, int64_t v)
     case GEMM_BF16_OPT_SERPENTINE: return v == 0 || v == 1;
     case GEMM_BF16_OPT_FAULT_TENSORMAP: return v == 0 || v == 1;
     case GEMM_BF16_OPT_THIN: return v >= 0 && v <= 2;
+    case GEMM_BF16_OPT_THIN_CLUSTER: return v >= 0 && v <= kThinMaxCluster;
     default: return false;
     }
 }
@@ -252,10 +256,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // 2-D bf16 tensor map: `cols` contiguous elements per row, `rows` rows,
-// `row_bytes` between rows; box = box_cols x box_rows with 128-byte swizzling;
-// out-of-bounds elements of a load read as zero.
+// `row_bytes` between rows; box = box_cols x box_rows, with 128-byte swizzling
+// unless `swizzle` is false (then the box is plain row-major in shared memory);
+// out-of-bounds elements of a load read as zero, those of a store are dropped.
 int encode_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t row_bytes, uint32_t box_cols,
-              uint32_t box_rows)
+              uint32_t box_rows, bool swizzle = true)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -265,7 +270,8 @@ int encode_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uin
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_BF16_OK : GEMM_BF16_ERR_TENSORMAP;
 }
@@ -469,6 +475,28 @@ int plan_square(gemm_bf16_t h, Plan &pl)
     return GEMM_BF16_OK;
 }
 
+// How many clusters of c thin-kernel CTAs can be resident at once (0 if none).
+int thin_max_active_clusters(const void *fn, int c, size_t smem, int threads)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)c, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // The thin kernel's plan (gemm_thin.cuh): the large operand in 128-row tiles,
 // the small one as the MMA's N side, one CTA per SM, the (tile, k-block) units
 // split evenly, and the workspace for the split tiles' partials.
@@ -512,7 +540,29 @@ int plan_thin(gemm_bf16_t h, Plan &pl)
     pl.threads = kThinThreads;
     if ((rc = prepare_kernel(pl.fn, h->max_smem_optin, &pl.regs)) != GEMM_BF16_OK)
         return rc;
-    pl.grid_ctas = (int)std::min<int64_t>(std::min<int64_t>(h->num_sms, kThinMaxGrid), pl.thin_units);
+    // Across the SMs, or one tile per cluster of C CTAs (gemm_thin.cuh).  The
+    // cluster form leaves SMs idle when tiles * C < SMs but has no split-tile
+    // traffic through global memory; on GB300 it was faster where tiles * C
+    // reaches ~60 % of the SMs and each CTA streams at most ~160 k-blocks
+    // (16x8192x8192: 28.9 -> ~26 us; 16x4096x8192: 14.7 -> ~11 us), slower on
+    // long runs (16x16384x16384, one CTA per tile: 91 -> 95 us).
+    const int64_t copt = h->opt[GEMM_BF16_OPT_THIN_CLUSTER];
+    const int64_t T = pl.tiles, KB = pl.num_k_blocks;
+    pl.thin_cluster = 0;
+    if (copt >= 2) {
+        pl.thin_cluster = (int)std::min<int64_t>(copt, KB);
+        if (pl.thin_cluster > 1 && thin_max_active_clusters(pl.fn, pl.thin_cluster, pl.smem, pl.threads) < 1)
+            return GEMM_BF16_ERR_UNSUPPORTED;
+    } else if (copt == 1 && T <= h->num_sms) {
+        int c = (int)std::min<int64_t>(std::min<int64_t>(kThinMaxCluster, h->num_sms / T), KB);
+        while (c > 1 && thin_max_active_clusters(pl.fn, c, pl.smem, pl.threads) < T)
+            --c;  // every cluster resident at once
+        if (T * c * 10 >= (int64_t)h->num_sms * 6 && (KB + c - 1) / c <= kThinClusterMaxKBlocks)
+            pl.thin_cluster = c;
+    }
+    pl.grid_ctas = pl.thin_cluster > 0
+                       ? (int)(T * pl.thin_cluster)
+                       : (int)std::min<int64_t>(std::min<int64_t>(h->num_sms, kThinMaxGrid), pl.thin_units);
     pl.sk_tiles = pl.sk_head = pl.sk_pieces = 0;
     pl.sk_units = 0;
     pl.sk_slots = 0;
@@ -803,6 +853,7 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
     info->k_order = p.k_order;
     info->serpentine = p.serpentine;
     info->thin = p.thin_nt;
+    info->thin_cluster = p.thin_cluster;
     return GEMM_BF16_OK;
 }
 
@@ -882,7 +933,14 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
     const int64_t small_rows = pl.thin_transposed ? pl.M : pl.N;
     const int64_t ld_large = pl.thin_transposed ? ops.ldb_e : ops.lda_e;
     const int64_t ld_small = pl.thin_transposed ? ops.lda_e : ops.ldb_e;
-    if (fault_maps || !h->maps_valid || h->mA != ops.Ae || h->mB != ops.Be) {
+    // Each CTA's last tile goes out by one TMA store when D allows it (16-byte
+    // aligned base and rows, and N a multiple of 8: a store clips D's columns
+    // only at 16-byte boundaries, so a box reaching past column N of a row
+    // with padding would write into the padding) and the epilogue is the
+    // plain one: a box of 128 columns by thin_nt rows of D (transposed) or
+    // thin_nt columns by 128 rows.
+    bool d_tma = !fz && (reinterpret_cast<uintptr_t>(D) & 15u) == 0 && (pl.ldd * 2) % 16 == 0 && pl.N % 8 == 0;
+    if (fault_maps || !h->maps_valid || h->mA != ops.Ae || h->mB != ops.Be || (d_tma && h->mD != D)) {
         if (fault_maps) {
             h->maps_valid = false;
             return GEMM_BF16_ERR_TENSORMAP;
@@ -894,7 +952,14 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
             h->maps_valid = false;
             return rc;
         }
-        h->mA = ops.Ae, h->mB = ops.Be, h->mD = nullptr;
+        // a D the driver will not describe is stored by the threads instead
+        if (d_tma && encode_2d(&h->tmD, D, (uint64_t)pl.N, (uint64_t)pl.M, (uint64_t)pl.ldd * 2,
+                               pl.thin_transposed ? (uint32_t)kBlockM : (uint32_t)pl.thin_nt,
+                               pl.thin_transposed ? (uint32_t)pl.thin_nt : (uint32_t)kBlockM, false) != GEMM_BF16_OK)
+            d_tma = false;
+        if (!d_tma)
+            std::memset(&h->tmD, 0, sizeof(h->tmD));  // passed, never used
+        h->mA = ops.Ae, h->mB = ops.Be, h->mD = d_tma ? D : nullptr;
         h->maps_valid = true;
     }
     if ((rc = launch_repacks(h, ops, st)) != GEMM_BF16_OK)
@@ -910,6 +975,7 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
     tp.transposed = pl.thin_transposed ? 1 : 0;
     tp.d_vec = ((reinterpret_cast<uintptr_t>(D) & 15u) == 0 && pl.ldd % 8 == 0) ? 1 : 0;
     tp.d_pair = ((reinterpret_cast<uintptr_t>(D) & 3u) == 0 && pl.ldd % 2 == 0) ? 1 : 0;
+    tp.d_tma = d_tma ? 1 : 0;
     tp.fault_skip_it = pl.fault_skip;
     tp.ldd = pl.ldd;
     tp.D = D;
@@ -918,6 +984,7 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
     tp.partials = h->thin_ws;
     tp.flags = h->thin_flags;
     tp.sync = h->thin_sync;
+    tp.cluster = pl.thin_cluster > 1 ? pl.thin_cluster : 1;
     tp.C = nullptr;
     tp.bias = nullptr;
     tp.ldc = 0;
@@ -940,7 +1007,7 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
     }
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     unsigned nattr = 0;
     cfg.gridDim = dim3((unsigned)pl.grid_ctas, 1, 1);
     cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
@@ -951,9 +1018,16 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
         attr[nattr].val.programmaticStreamSerializationAllowed = 1;
         ++nattr;
     }
+    if (tp.cluster > 1) {
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = (unsigned)tp.cluster;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+    }
     cfg.attrs = nattr ? attr : nullptr;
     cfg.numAttrs = nattr;
-    void *args[3] = {&h->tmA, &h->tmB, &tp};
+    void *args[4] = {&h->tmA, &h->tmB, &h->tmD, &tp};
     if (cudaLaunchKernelExC(&cfg, pl.fn, args) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_BF16_ERR_CUDA;

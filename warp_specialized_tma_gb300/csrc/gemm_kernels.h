@@ -100,6 +100,8 @@ inline size_t nows_smem_bytes(int stages)
 constexpr int kThinThreads = 256;  // warp 0 producer, 1 MMA, 2 TMEM allocation, 4-7 epilogue
 constexpr int kThinMaxStages = 12;
 constexpr int kThinMaxRows = 64;
+constexpr int kThinMaxCluster = 8;            // portable cluster size limit
+constexpr int64_t kThinClusterMaxKBlocks = 160;  // automatic cluster form: k-blocks per CTA at most
 
 struct ThinParams {
     int32_t rows;           // rows of the large operand
@@ -111,6 +113,7 @@ struct ThinParams {
     int32_t transposed;     // 1: the large operand is B, so D[m][n] is accumulator row n, column m
     int32_t d_vec;          // 1: rows of D are 16-byte aligned (vector stores, not transposed only)
     int32_t d_pair;         // 1: rows of D are 4-byte aligned (paired stores, transposed only)
+    int32_t d_tma;          // 1: each CTA's last tile is stored by TMA (tensor map of D; not fused)
     int32_t fault_skip_it;  // test hook, -1 = off
     int64_t ldd;
     void *D;
@@ -119,6 +122,9 @@ struct ThinParams {
     float *partials;        // 2 slots per CTA, 128 x NT fp32 each
     uint32_t *flags;        // 4 per slot (one per epilogue warp): == epoch once that warp's rows are stored
     uint32_t *sync;         // {epoch (never 0), CTAs that have read it}, advanced on the device
+    int32_t cluster;        // > 1: clusters of this many CTAs split each tile's k-blocks (one tile per
+                            // cluster, partials summed through distributed shared memory); 1: the
+                            // units are split across the CTAs (thin_split.h)
     // fused epilogue, as in GemmParams
     const void *C;
     const void *bias;
@@ -141,7 +147,7 @@ inline size_t thin_smem_bytes(int nt, int stages)
 const void *ws_kernel_c1(bool setmaxnreg);
 const void *ws_kernel_c2(bool setmaxnreg);
 const void *nows_kernel(bool mbar_war);
-// (CUtensorMap large, CUtensorMap small, ThinParams); nt = 16, 32, 48 or 64.
+// (CUtensorMap large, CUtensorMap small, CUtensorMap D, ThinParams); nt = 16, 32, 48 or 64.
 const void *thin_kernel(int nt);
 
 // One operand copy: `rows` rows of `cols` bf16 from pitch ld_src to pitch

@@ -22,8 +22,20 @@
 //                    fp32 partials and stores the tile (thin_split.h)
 // Every wait is bounded by the watchdog (WaitCtl in ptx.cuh).
 //
-// A split tile's pieces meet through fp32 partials in a workspace and one flag
-// per partial slot and epilogue warp.  A contributor warp stores its 32 rows,
+// Two ways to split the work.  Across the SMs (the default for large or long
+// problems): the (tile, k-block) units are cut into one contiguous range per
+// CTA, and a split tile's pieces meet through global memory, as follows.  In
+// clusters (problems whose tiles times a cluster size of 2..8 nearly fill the
+// GPU): the C CTAs of cluster c split tile c's k-blocks evenly, rank r > 0
+// leaves its fp32 partial in its own shared memory (the drained ring) and
+// arrives, per epilogue warp, on a barrier of rank 0 with release at cluster
+// scope; rank 0's warp waits on it (bounded), reads the rows of ranks 1..C-1
+// through distributed shared memory in rank order, adds, and stores.  A
+// cluster barrier at exit keeps every rank's shared memory alive until rank 0
+// has read it.  One CTA per whole tile is the cluster form with C = 1.
+//
+// Across the SMs, a split tile's pieces meet through fp32 partials in a
+// workspace and one flag per partial slot and epilogue warp.  A contributor warp stores its 32 rows,
 // meets at a warp barrier, and its lane 0 writes the launch's epoch to the
 // flag with a release store; the owner warp's lane 0 polls the flag with
 // acquire loads, the warp meets at a warp barrier, and the 32 lanes read the
@@ -141,10 +153,54 @@ __device__ __forceinline__ void thin_store_row(const float (&v)[NT], int64_t r, 
             row[i] = thin_bf16(thin_epilogue_value(v[i], r, i, p));
 }
 
+// Writes one accumulator row (row_in_tile of the tile) as bf16 into the staging
+// buffer of the tile's TMA store.  Transposed: the box is 128 columns of D by
+// NT rows, so D row i holds this row's value i at column row_in_tile; else the
+// box is NT columns by 128 rows, this row's NT values contiguous.
+template <int NT>
+__device__ __forceinline__ void thin_stage_row(const float (&v)[NT], int row_in_tile, uint32_t stage, bool transposed)
+{
+    if (transposed) {
+#pragma unroll
+        for (int i = 0; i < NT; ++i)
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stage + (uint32_t)(i * kBlockM + row_in_tile) * 2u),
+                         "h"(thin_bf16(v[i]))
+                         : "memory");
+        return;
+    }
+    const uint32_t row = stage + (uint32_t)(row_in_tile * NT) * 2u;
+#pragma unroll
+    for (int i = 0; i < NT; i += 8)
+        st_shared_v4(row + (uint32_t)i * 2u, pack_bf16x2(__float_as_uint(v[i]), __float_as_uint(v[i + 1])),
+                     pack_bf16x2(__float_as_uint(v[i + 2]), __float_as_uint(v[i + 3])),
+                     pack_bf16x2(__float_as_uint(v[i + 4]), __float_as_uint(v[i + 5])),
+                     pack_bf16x2(__float_as_uint(v[i + 6]), __float_as_uint(v[i + 7])));
+}
+
+// Stores a CTA's last tile: every epilogue thread stages its row in the ring
+// (drained: the CTA has no loads or MMAs left), the four warps meet, and one
+// thread issues the tile's TMA store and waits until it has read the staging.
+// The TMA engine writes whole lines of D, where per-thread stores of a
+// transposed tile write 64-byte pieces of NT rows at once in every CTA.
+template <int NT>
+__device__ __forceinline__ void thin_store_tile_tma(const float (&v)[NT], int row_in_tile, int64_t t, uint32_t stage,
+                                                    const CUtensorMap *tmD, const ThinParams &p)
+{
+    thin_stage_row<NT>(v, row_in_tile, stage, p.transposed != 0);
+    fence_proxy_async_shared();  // the staging writes come before the async-proxy read
+    named_barrier_sync(1u, 128u);
+    if (threadIdx.x == 128) {
+        const int32_t at = (int32_t)(t * kBlockM);
+        tma_store_2d(tmD, stage, p.transposed ? at : 0, p.transposed ? 0 : at);
+        bulk_commit_group();
+        bulk_wait_read_all();
+    }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kThinThreads, 1)
     gemm_thin_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmS,
-                     const ThinParams p)
+                     const __grid_constant__ CUtensorMap tmD, const ThinParams p)
 {
     static_assert(NT % 16 == 0 && NT >= 16 && NT <= kThinMaxRows, "NT: 16, 32, 48 or 64");
     constexpr uint32_t kLBytes = (uint32_t)kBlockM * kBlockK * 2;  // 128 rows of the large operand
@@ -163,7 +219,8 @@ __global__ void __launch_bounds__(kThinThreads, 1)
     const uint32_t accf_bar = empty_bar + 8u * S;
     const uint32_t acce_bar = accf_bar + 16u;
     const uint32_t done_bar = acce_bar + 16u;
-    const uint32_t tmem_slot = done_bar + 8u;
+    const uint32_t ready_bar = done_bar + 8u;  // 4, one per epilogue warp (rank 0 of a cluster)
+    const uint32_t tmem_slot = ready_bar + 32u;
     const uint32_t abort_flag = tmem_slot + 4u;
     const uint32_t epoch_word = abort_flag + 4u;
     const uint32_t go_words = epoch_word + 4u;  // 2 words, alternating by item
@@ -181,6 +238,9 @@ __global__ void __launch_bounds__(kThinThreads, 1)
             mbar_init(acce_bar + 8u * a, 4);  // one arrival per epilogue warp
         }
         mbar_init(done_bar, 1);
+        if (p.cluster > 1)
+            for (int q = 0; q < 4; ++q)
+                mbar_init(ready_bar + 8u * q, (uint32_t)p.cluster - 1u);  // one arrival per other rank
         st_shared_u32(abort_flag, 0u);
         fence_mbarrier_init();
     }
@@ -188,7 +248,12 @@ __global__ void __launch_bounds__(kThinThreads, 1)
         prefetch_tensormap(&tmL);
         prefetch_tensormap(&tmS);
     }
-    __syncthreads();
+    if (p.cluster > 1) {
+        __syncwarp();
+        cluster_arrive_wait();  // every rank's barriers are initialised before any remote arrive
+    } else {
+        __syncthreads();
+    }
     if (warp == 2) {
         tmem_alloc<1>(tmem_slot, kAllocCols);
         tmem_relinquish<1>();
@@ -359,8 +424,55 @@ __global__ void __launch_bounds__(kThinThreads, 1)
                 acc_ph ^= 1u;
 
             const int64_t r = t * kBlockM + row_in_tile;
-            if (kb0 == 0 && kb1 == KB) {
-                thin_store_row<NT>(v, r, p);  // this range holds the whole tile
+            // the CTA's last item is stored by TMA from the drained ring
+            const bool tma_store = p.d_tma && t == t_last;
+            if (kb0 == 0 && kb1 == KB) {  // this range holds the whole tile
+                if (tma_store)
+                    thin_store_tile_tma<NT>(v, row_in_tile, t, stage0, &tmD, p);
+                else
+                    thin_store_row<NT>(v, r, p);
+                continue;
+            }
+            if (p.cluster > 1) {
+                // Cluster form: this CTA's only item is rank r's share of tile c.
+                // The ring is drained (every load landed, and the MMAs that read
+                // it completed before the accumulator was handed over), so its
+                // first bytes hold the partial, as float4 columns of 128 rows.
+                const uint32_t part = stage0 + (uint32_t)row_in_tile * 16u;
+                if (kb0 > 0) {
+#pragma unroll
+                    for (int i = 0; i < NT; i += 4)
+                        st_shared_v4(part + (uint32_t)((i >> 2) * kBlockM) * 16u, __float_as_uint(v[i]),
+                                     __float_as_uint(v[i + 1]), __float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
+                    __syncwarp();  // the warp's stores come before lane 0's release
+                    if (lane == 0)
+                        mbar_arrive_cluster(mapa_shared(ready_bar + 8u * (uint32_t)q, 0u));
+                    continue;
+                }
+                uint32_t ok = 1u;
+                if (lane == 0)
+                    ok = ctl.wait<true>(ready_bar + 8u * (uint32_t)q, 0u, kRoleFixup, (uint32_t)q) ? 1u : 0u;
+                __syncwarp();  // lane 0's acquire comes before the lanes' loads
+                // if the watchdog gave up, the rows are stored unsummed (the
+                // status says so): every warp still reaches the store
+                const bool have_parts = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0u;
+                for (int rk = 1; have_parts && rk < p.cluster; ++rk) {
+                    // all of a rank's loads first, then the adds: a remote
+                    // round trip each, overlapped rather than one after another
+                    const uint32_t rp = mapa_shared(part, (uint32_t)rk);
+                    uint32_t w[NT];
+#pragma unroll
+                    for (int i = 0; i < NT; i += 4)
+                        ld_shared_cluster_v4(rp + (uint32_t)((i >> 2) * kBlockM) * 16u, w[i], w[i + 1], w[i + 2],
+                                             w[i + 3]);
+#pragma unroll
+                    for (int i = 0; i < NT; ++i)
+                        v[i] += __uint_as_float(w[i]);
+                }
+                if (tma_store)
+                    thin_store_tile_tma<NT>(v, row_in_tile, t, stage0, &tmD, p);
+                else
+                    thin_store_row<NT>(v, r, p);
                 continue;
             }
             // A piece of a split tile.  The piece that holds k-block 0 owns the
@@ -406,13 +518,21 @@ __global__ void __launch_bounds__(kThinThreads, 1)
                     v[i + 3] += f.w;
                 }
             }
-            thin_store_row<NT>(v, r, p);
+            if (tma_store)
+                thin_store_tile_tma<NT>(v, row_in_tile, t, stage0, &tmD, p);
+            else
+                thin_store_row<NT>(v, r, p);
         }
     }
 
     // ---------------- teardown ----------------
     tc_fence_before_sync();
-    __syncthreads();
+    if (p.cluster > 1) {
+        __syncwarp();
+        cluster_arrive_wait();  // rank 0 may still read the others' shared memory
+    } else {
+        __syncthreads();
+    }
     if (warp == 2) {
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, kAllocCols);

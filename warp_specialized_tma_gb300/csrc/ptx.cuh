@@ -73,6 +73,15 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint32_t a, 
                  : "memory");
 }
 
+// Load from a (possibly peer CTA's) shared::cluster address.
+__device__ __forceinline__ void ld_shared_cluster_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d)
+{
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "r"(addr)
+                 : "memory");
+}
+
 // Store to a (possibly peer CTA's) shared::cluster address.
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
 {
