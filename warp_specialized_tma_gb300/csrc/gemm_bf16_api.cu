@@ -53,6 +53,7 @@ struct Plan {
     int thin_nt = 0;                          // > 0: the thin kernel, small-operand width 16..64
     bool thin_transposed = false;             // thin kernel: the large operand is B
     int64_t thin_units = 0;                   // thin kernel: tiles * k-blocks
+    int thin_push = 0;                        // thin cluster form: partials stored into rank 0
     int thin_cluster = 0;                     // thin kernel: 0 = units split across the SMs, else
                                               // CTAs per tile (1 = whole tiles, > 1 = a cluster)
     int64_t tiles = 0;
@@ -563,6 +564,16 @@ int plan_thin(gemm_bf16_t h, Plan &pl)
     pl.grid_ctas = pl.thin_cluster > 0
                        ? (int)(T * pl.thin_cluster)
                        : (int)std::min<int64_t>(std::min<int64_t>(h->num_sms, kThinMaxGrid), pl.thin_units);
+    // Where rank 0's shared memory has room beside the ring for the other
+    // ranks' partials, they store them there (no remote reads at the end).
+    pl.thin_push = 0;
+    if (pl.thin_cluster > 1) {
+        const size_t recv = (size_t)(pl.thin_cluster - 1) * kBlockM * (size_t)pl.thin_nt * sizeof(float);
+        if (pl.smem + recv <= h->max_smem_optin) {
+            pl.thin_push = 1;
+            pl.smem += recv;
+        }
+    }
     pl.sk_tiles = pl.sk_head = pl.sk_pieces = 0;
     pl.sk_units = 0;
     pl.sk_slots = 0;
@@ -985,6 +996,7 @@ int run_thin(gemm_bf16_t h, const OperandView &ops, void *D, const FusedArgs *fz
     tp.flags = h->thin_flags;
     tp.sync = h->thin_sync;
     tp.cluster = pl.thin_cluster > 1 ? pl.thin_cluster : 1;
+    tp.push = pl.thin_push;
     tp.C = nullptr;
     tp.bias = nullptr;
     tp.ldc = 0;

@@ -125,6 +125,8 @@ struct ThinParams {
     int32_t cluster;        // > 1: clusters of this many CTAs split each tile's k-blocks (one tile per
                             // cluster, partials summed through distributed shared memory); 1: the
                             // units are split across the CTAs (thin_split.h)
+    int32_t push;           // cluster form: 1 = ranks 1..C-1 store their partials into rank 0's
+                            // receive area after its barriers ((C - 1) x 128 x NT fp32), 0 = rank 0 reads them
     // fused epilogue, as in GemmParams
     const void *C;
     const void *bias;

@@ -30,9 +30,11 @@
 // leaves its fp32 partial in its own shared memory (the drained ring) and
 // arrives, per epilogue warp, on a barrier of rank 0 with release at cluster
 // scope; rank 0's warp waits on it (bounded), reads the rows of ranks 1..C-1
-// through distributed shared memory in rank order, adds, and stores.  A
-// cluster barrier at exit keeps every rank's shared memory alive until rank 0
-// has read it.  One CTA per whole tile is the cluster form with C = 1.
+// through distributed shared memory in rank order, adds, and stores.  Where
+// rank 0's shared memory has room for the others' partials beside a full ring,
+// they store them there instead (remote stores, which do not wait) and rank 0
+// reads its own shared memory.  A cluster barrier at exit keeps every rank's
+// shared memory alive until rank 0 has read it.  One CTA per whole tile is the cluster form with C = 1.
 //
 // Across the SMs, a split tile's pieces meet through fp32 partials in a
 // workspace and one flag per partial slot and epilogue warp.  A contributor warp stores its 32 rows,
@@ -224,6 +226,9 @@ __global__ void __launch_bounds__(kThinThreads, 1)
     const uint32_t abort_flag = tmem_slot + 4u;
     const uint32_t epoch_word = abort_flag + 4u;
     const uint32_t go_words = epoch_word + 4u;  // 2 words, alternating by item
+    // cluster form with push: ranks 1..C-1's partials, one 128 x NT fp32 slot each
+    const uint32_t recv = stage0 + (uint32_t)S * kStageBytes + 512u;
+    constexpr uint32_t kPartBytes = (uint32_t)kBlockM * NT * 4u;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -440,10 +445,21 @@ __global__ void __launch_bounds__(kThinThreads, 1)
                 // first bytes hold the partial, as float4 columns of 128 rows.
                 const uint32_t part = stage0 + (uint32_t)row_in_tile * 16u;
                 if (kb0 > 0) {
+                    if (p.push) {
+                        const uint32_t dst = mapa_shared(
+                            recv + (cluster_ctarank() - 1u) * kPartBytes + (uint32_t)row_in_tile * 16u, 0u);
 #pragma unroll
-                    for (int i = 0; i < NT; i += 4)
-                        st_shared_v4(part + (uint32_t)((i >> 2) * kBlockM) * 16u, __float_as_uint(v[i]),
-                                     __float_as_uint(v[i + 1]), __float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
+                        for (int i = 0; i < NT; i += 4)
+                            st_shared_cluster_v4(dst + (uint32_t)((i >> 2) * kBlockM) * 16u, __float_as_uint(v[i]),
+                                                 __float_as_uint(v[i + 1]), __float_as_uint(v[i + 2]),
+                                                 __float_as_uint(v[i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < NT; i += 4)
+                            st_shared_v4(part + (uint32_t)((i >> 2) * kBlockM) * 16u, __float_as_uint(v[i]),
+                                         __float_as_uint(v[i + 1]), __float_as_uint(v[i + 2]),
+                                         __float_as_uint(v[i + 3]));
+                    }
                     __syncwarp();  // the warp's stores come before lane 0's release
                     if (lane == 0)
                         mbar_arrive_cluster(mapa_shared(ready_bar + 8u * (uint32_t)q, 0u));
@@ -459,12 +475,19 @@ __global__ void __launch_bounds__(kThinThreads, 1)
                 for (int rk = 1; have_parts && rk < p.cluster; ++rk) {
                     // all of a rank's loads first, then the adds: a remote
                     // round trip each, overlapped rather than one after another
-                    const uint32_t rp = mapa_shared(part, (uint32_t)rk);
                     uint32_t w[NT];
+                    if (p.push) {
+                        const uint32_t lp = recv + (uint32_t)(rk - 1) * kPartBytes + (uint32_t)row_in_tile * 16u;
 #pragma unroll
-                    for (int i = 0; i < NT; i += 4)
-                        ld_shared_cluster_v4(rp + (uint32_t)((i >> 2) * kBlockM) * 16u, w[i], w[i + 1], w[i + 2],
-                                             w[i + 3]);
+                        for (int i = 0; i < NT; i += 4)
+                            ld_shared_v4(lp + (uint32_t)((i >> 2) * kBlockM) * 16u, w[i], w[i + 1], w[i + 2], w[i + 3]);
+                    } else {
+                        const uint32_t rp = mapa_shared(part, (uint32_t)rk);
+#pragma unroll
+                        for (int i = 0; i < NT; i += 4)
+                            ld_shared_cluster_v4(rp + (uint32_t)((i >> 2) * kBlockM) * 16u, w[i], w[i + 1], w[i + 2],
+                                                 w[i + 3]);
+                    }
 #pragma unroll
                     for (int i = 0; i < NT; ++i)
                         v[i] += __uint_as_float(w[i]);
