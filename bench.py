@@ -445,10 +445,12 @@ def run_reference(args):
 
 
 def measure_shape(M, N, K, dist, seed, dev, stream, peaks, peak_src, flush_buf, label,
-                  cpu_seconds=None, graph_too=False, hbm_comparator=False):
+                  cpu_seconds=None, graph_too=False, hbm_comparator=False, library_comparator=False):
     """One problem through the C ABI: plan, warm up, time.  Inputs larger than
     L2 are timed back to back; smaller ones launch by launch with an L2 flush
-    before each.  Returns a dict for the bench line's detail block."""
+    before each.  With library_comparator, torch.matmul (cuBLAS) on the same
+    operands is timed the same way afterwards.  Returns a dict for the bench
+    line's detail block."""
     import torch
     from warp_specialized_tma_gb300 import binding, inputs
     A, B = inputs.make_problem(M, N, K, dist, seed)
@@ -525,6 +527,27 @@ def measure_shape(M, N, K, dist, seed, dev, stream, peaks, peak_src, flush_buf, 
                                           "back to back", "us": cms * 1e3, "gbs": cgbs,
                                   "ours_over_copy": gbs / cgbs}
         del src, dst
+    if library_comparator:
+        # Not an oracle and not part of the library: the vendor GEMM on the same
+        # operands under the same timing protocol, for context.
+        dD2 = torch.empty_like(dD)
+
+        def lib_run():
+            torch.matmul(dA, dB.t(), out=dD2)
+
+        for _ in range(5):
+            lib_run()
+        torch.cuda.synchronize(dev)
+        if big:
+            lms = time_back_to_back(lib_run, n, stream, dev)
+        else:
+            lms = statistics.fmean(time_each_flushed(lib_run, min(n, 200), stream, dev, flush_buf))
+        out["library_comparator"] = {"what": "torch.matmul(A, B.T) (cuBLAS), same operands, same protocol ("
+                                             + l2 + "), timed after ours",
+                                     "us_per_launch": lms * 1e3,
+                                     "tflops": roof["flops"] / (lms * 1e-3) / 1e12,
+                                     "ours_over_library_time": ms / lms}
+        del dD2
     if graph_us is not None:
         out["graph_replay_us_per_launch"] = graph_us
         out["graph_replay_note"] = "200 launches replayed from one CUDA graph, back to back (inputs stay in L2)"
@@ -751,11 +774,13 @@ def run_ours(args):
                 continue
             workloads[name] = measure_shape(wl["M"], wl["N"], wl["K"], wl["dist"], wl["seed"], dev, stream,
                                             peaks, peak_src, flush_buf, name,
-                                            cpu_seconds=args.cpu_seconds_detail, graph_too=(name == "cube256"))
+                                            cpu_seconds=args.cpu_seconds_detail, graph_too=(name == "cube256"),
+                                            library_comparator=args.comparator)
         skinny = {}
         for (m, n_, k) in SKINNY_SHAPES:
             skinny[f"{m}x{n_}x{k}"] = measure_shape(m, n_, k, "uniform", 3, dev, stream, peaks, peak_src,
-                                                    flush_buf, f"{m}x{n_}x{k}", hbm_comparator=True)
+                                                    flush_buf, f"{m}x{n_}x{k}", hbm_comparator=True,
+                                                    library_comparator=args.comparator)
 
     if dist.rank == 0:
         line = {
