@@ -79,7 +79,10 @@ typedef enum gemm_bf16_pipeline {
 /* Options, set before gemm_bf16_plan (a later plan picks them up). */
 typedef enum gemm_bf16_option {
     GEMM_BF16_OPT_PIPELINE = 1,      /* gemm_bf16_pipeline; default GEMM_BF16_PIPE_WS */
-    GEMM_BF16_OPT_CTA_GROUP = 2,     /* 0 = automatic (default), 1 = one SM per tile (128x256),
+    GEMM_BF16_OPT_CTA_GROUP = 2,     /* 0 = automatic (default: an SM pair, except one SM for
+                                        problems of at most 512 x 512 outputs and 512^3
+                                        multiply-adds, which are bound by fixed latency),
+                                        1 = one SM per tile (128x256),
                                         2 = SM pair per tile (256x256, cta_group::2, WS only) */
     GEMM_BF16_OPT_PERSISTENT = 3,    /* 1 (default): grid = resident CTAs, grid-stride tile loop;
                                         0: one tile per CTA (grid = tiles) */

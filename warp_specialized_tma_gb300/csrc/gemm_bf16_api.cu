@@ -319,7 +319,12 @@ int plan_square(gemm_bf16_t h, Plan &pl)
         pl.sched_dynamic = 0;
         pl.k_order = 0;
     } else if (cg == 0) {
-        cg = 2;  // an SM pair per 256x256 tile halves each SM's operand traffic
+        // An SM pair per 256x256 tile halves each SM's operand traffic.  Problems
+        // of at most 512^3 multiply-adds are bound by fixed latency instead, and
+        // the single-CTA kernel (no cluster barriers, half the epilogue per CTA)
+        // measured faster there: 256^3 10.8 against 12.1 us, 512^3 12.3 against
+        // 12.7 us, with L2 flushed (1024^3: 16.4 against 16.0).
+        cg = (M * N <= (int64_t)512 * 512 && M * N * K <= (int64_t)512 * 512 * 512) ? 1 : 2;
     }
     pl.cta_group = cg;
     if (pl.epi_pingpong && pl.acc_buffers != 2)
