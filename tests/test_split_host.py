@@ -42,8 +42,9 @@ def test_work_split_and_tile_order(tmp_path):
 
 def test_thin_kernel_work_split(tmp_path):
     """The thin kernel's split (csrc/thin_split.h, plain C++): ranges, pieces,
-    partial slots and the epoch-tagged tile counter, checked by
-    tests/thin_split_check.cpp.  Needs a C++ compiler, not a GPU."""
+    partial slots and owners, the cluster form's ranges, and the automatic
+    cluster size on a model of GB300, checked by tests/thin_split_check.cpp.
+    Needs a C++ compiler, not a GPU."""
     cxx = shutil.which("g++") or shutil.which("c++")
     if cxx is None:
         pytest.skip("no C++ compiler")

@@ -8,7 +8,12 @@
 // that no two pieces share a slot; and that the owner of each split tile (the
 // piece holding its k-block 0, range_of(t * KB)) is the last tile of its range,
 // so that an owner never waits for anything before its own last item, and the
-// other pieces are not.
+// other pieces are not.  For the cluster form (G = T * C, C <= KB) it checks
+// that cluster c's C ranges lie in tile c with rank r holding k-blocks
+// [floor(r KB / C), floor((r + 1) KB / C)); and it checks the automatic cluster
+// size against a device model of 8 clusters-capable groups of 19 SMs: fixed
+// cases, and on a sweep that the choice meets every condition and no larger
+// size would.
 // Prints "ok" and exits 0, or prints the first failure and exits 1.
 #include <cstdio>
 #include <set>
@@ -77,11 +82,84 @@ void check_split(int64_t T, int32_t KB, int32_t G)
     }
 }
 
+void check_cluster_split(int64_t T, int32_t KB, int32_t C)
+{
+    const int64_t U = T * KB;
+    const int32_t G = (int32_t)(T * C);
+    for (int64_t c = 0; c < T; ++c)
+        for (int32_t r = 0; r < C; ++r) {
+            const int32_t j = (int32_t)(c * C + r);
+            const int64_t b = thin_begin(U, G, j), e = thin_begin(U, G, j + 1);
+            CHECK(b == c * KB + (int64_t)r * KB / C && e == c * KB + (int64_t)(r + 1) * KB / C,
+                  "T=%lld KB=%d C=%d: rank %d of cluster %lld holds [%lld, %lld)", (long long)T, KB, C, r,
+                  (long long)c, (long long)b, (long long)e);
+            CHECK(e > b, "T=%lld KB=%d C=%d: rank %d of cluster %lld is empty", (long long)T, KB, C, r, (long long)c);
+        }
+}
+
+// resident[c]: clusters of c CTAs (one CTA per SM) that fit at once on 8 groups
+// of 19 SMs, a cluster never spanning two groups
+void gb300_model(int32_t (&resident)[kThinMaxCluster + 1])
+{
+    resident[0] = 0;
+    resident[1] = 152;
+    for (int c = 2; c <= kThinMaxCluster; ++c)
+        resident[c] = 8 * (19 / c);
+}
+
+void check_auto_cluster_case(int64_t T, int64_t KB, int32_t want)
+{
+    int32_t resident[kThinMaxCluster + 1];
+    gb300_model(resident);
+    const int32_t got = thin_auto_cluster(T, KB, 152, resident);
+    CHECK(got == want, "T=%lld KB=%lld: cluster %d, expected %d", (long long)T, (long long)KB, got, want);
+}
+
+void check_auto_cluster_sweep()
+{
+    int32_t resident[kThinMaxCluster + 1];
+    gb300_model(resident);
+    const int32_t sms = 152;
+    for (int64_t T = 1; T <= 300; ++T)
+        for (int64_t KB : {1, 2, 3, 5, 8, 16, 33, 64, 128, 160, 161, 256, 320, 512}) {
+            const int32_t c = thin_auto_cluster(T, KB, sms, resident);
+            if (c == 0)
+                continue;
+            CHECK(c >= 1 && c <= kThinMaxCluster && c <= KB && T * c <= sms, "T=%lld KB=%lld: cluster %d out of range",
+                  (long long)T, (long long)KB, c);
+            CHECK(c == 1 || resident[c] >= T, "T=%lld: %d clusters of %d do not fit at once", (long long)T, (int)T, c);
+            CHECK(T * c * 10 >= (int64_t)sms * 6, "T=%lld C=%d fills less than 60 %% of the SMs", (long long)T, c);
+            CHECK((KB + c - 1) / c <= kThinClusterMaxKBlocks, "T=%lld KB=%lld C=%d: runs too long", (long long)T,
+                  (long long)KB, c);
+            for (int32_t d = c + 1; d <= kThinMaxCluster && d <= KB && T * d <= sms; ++d)
+                CHECK(resident[d] < T, "T=%lld KB=%lld: cluster %d chosen but %d also fits", (long long)T,
+                      (long long)KB, c, d);
+        }
+}
+
 }  // namespace
 
 int main()
 {
     long n = 0;
+    for (int64_t T = 1; T <= 40; ++T)
+        for (int32_t KB : {1, 2, 3, 7, 16, 65, 128})
+            for (int32_t C = 1; C <= kThinMaxCluster && C <= KB; ++C) {
+                check_cluster_split(T, KB, C);
+                ++n;
+            }
+    // the decode-like shapes of the bench and the tests (tiles of 128 rows, k-blocks of 64)
+    check_auto_cluster_case(64, 128, 2);    // 16 x 8192 x 8192
+    check_auto_cluster_case(32, 128, 4);    // 16 x 4096 x 8192
+    check_auto_cluster_case(32, 32, 4);     // 16 x 4096 x 2048
+    check_auto_cluster_case(96, 128, 1);    // 16 x 12288 x 8192: whole tiles
+    check_auto_cluster_case(128, 256, 0);   // 16 x 16384 x 16384: 256 k-blocks per CTA
+    check_auto_cluster_case(224, 128, 0);   // 16 x 28672 x 8192: more tiles than SMs
+    check_auto_cluster_case(8, 8, 0);       // 16 x 1024 x 512: too few CTAs
+    check_auto_cluster_case(20, 128, 6);    // 7 per cluster would leave clusters waiting
+    check_auto_cluster_case(64, 1, 0);      // one k-block: whole tiles on 64 SMs only
+    check_auto_cluster_sweep();
+    n += 10;
     for (int64_t T = 1; T <= 24; ++T)
         for (int32_t KB : {1, 2, 3, 7, 16, 65, 128})
             for (int32_t G : {1, 2, 3, 5, 8, 13, 33, 76, 152})

@@ -560,11 +560,11 @@ int plan_thin(gemm_bf16_t h, Plan &pl)
         if (pl.thin_cluster > 1 && thin_max_active_clusters(pl.fn, pl.thin_cluster, pl.smem, pl.threads) < 1)
             return GEMM_BF16_ERR_UNSUPPORTED;
     } else if (copt == 1 && T <= h->num_sms) {
-        int c = (int)std::min<int64_t>(std::min<int64_t>(kThinMaxCluster, h->num_sms / T), KB);
-        while (c > 1 && thin_max_active_clusters(pl.fn, c, pl.smem, pl.threads) < T)
-            --c;  // every cluster resident at once
-        if (T * c * 10 >= (int64_t)h->num_sms * 6 && (KB + c - 1) / c <= kThinClusterMaxKBlocks)
-            pl.thin_cluster = c;
+        int32_t resident[kThinMaxCluster + 1] = {0};
+        resident[1] = h->num_sms;  // one CTA per SM
+        for (int c = 2; c <= kThinMaxCluster && c <= KB && c * T <= h->num_sms; ++c)
+            resident[c] = thin_max_active_clusters(pl.fn, c, pl.smem, pl.threads);
+        pl.thin_cluster = thin_auto_cluster(T, KB, h->num_sms, resident);
     }
     pl.grid_ctas = pl.thin_cluster > 0
                        ? (int)(T * pl.thin_cluster)

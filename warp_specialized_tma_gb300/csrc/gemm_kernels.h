@@ -100,8 +100,6 @@ inline size_t nows_smem_bytes(int stages)
 constexpr int kThinThreads = 256;  // warp 0 producer, 1 MMA, 2 TMEM allocation, 4-7 epilogue
 constexpr int kThinMaxStages = 12;
 constexpr int kThinMaxRows = 64;
-constexpr int kThinMaxCluster = 8;            // portable cluster size limit
-constexpr int64_t kThinClusterMaxKBlocks = 160;  // automatic cluster form: k-blocks per CTA at most
 
 struct ThinParams {
     int32_t rows;           // rows of the large operand

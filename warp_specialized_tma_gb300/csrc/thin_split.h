@@ -51,4 +51,34 @@ WSTMA_THIN_FN int32_t thin_slot(int64_t U, int32_t G, int32_t KB, int32_t j, int
 // The grid is one CTA per SM; this bounds the partial slots (2 per CTA).
 constexpr int32_t kThinMaxGrid = 1024;
 
+// The cluster form (gemm_thin.cuh) is the split above with G = T * C: every
+// C-th range starts at a tile boundary (begin(c C) = c KB exactly), so cluster
+// c's C ranges lie in tile c, rank r holding k-blocks [floor(r KB / C),
+// floor((r + 1) KB / C)), rank 0 holding k-block 0.  C <= KB keeps every range
+// non-empty.
+constexpr int32_t kThinMaxCluster = 8;            // portable cluster size limit
+constexpr int64_t kThinClusterMaxKBlocks = 160;  // automatic cluster form: k-blocks per CTA at most
+
+// The automatic choice: the largest C <= kThinMaxCluster with T * C <= sms,
+// C <= KB and all T clusters of C resident at once (resident[C] >= T, where
+// resident[c] is how many clusters of c CTAs fit on the device, c = 1..8);
+// taken when T * C reaches 60 % of the SMs and each CTA streams at most
+// kThinClusterMaxKBlocks k-blocks.  Returns C (1 = one CTA per whole tile), or
+// 0 for the split across the SMs.
+WSTMA_THIN_FN int32_t thin_auto_cluster(int64_t T, int64_t KB, int32_t sms, const int32_t *resident)
+{
+    if (T < 1 || KB < 1 || T > sms)
+        return 0;
+    int64_t c = sms / T;
+    if (c > kThinMaxCluster)
+        c = kThinMaxCluster;
+    if (c > KB)
+        c = KB;
+    while (c > 1 && resident[c] < T)
+        --c;
+    if (T * c * 10 >= (int64_t)sms * 6 && (KB + c - 1) / c <= kThinClusterMaxKBlocks)
+        return (int32_t)c;
+    return 0;
+}
+
 }  // namespace wstma
