@@ -175,11 +175,13 @@ typedef enum gemm_bf16_option {
                                         streaming the other operand from HBM) can run on the thin
                                         kernel: the large operand in 128-row tiles is the MMA's M
                                         side, the small one its N side (rounded up to 16, 32, 48 or
-                                        64), one CTA per SM with a ring of up to 12 stages, the
-                                        (tile, k-block) units split evenly over the SMs, and split
-                                        tiles summed in a fixed order from fp32 partials in a
-                                        handle-owned workspace (2 slots of 128 x 64 fp32 per SM,
-                                        4 flags per slot, and two words).  Of the other options only
+                                        64), at most one CTA per SM with a ring of up to 12 stages;
+                                        each tile's k-blocks split over a thread-block cluster, or
+                                        the (tile, k-block) units split evenly over the SMs
+                                        (GEMM_BF16_OPT_THIN_CLUSTER); split tiles summed in a fixed
+                                        order, across the SMs from fp32 partials in a handle-owned
+                                        workspace (2 slots of 128 x 64 fp32 per SM, 4 flags per
+                                        slot, and two words).  Of the other options only
                                         WATCHDOG_NS, FAULT_SKIP_LOAD, PDL, REPACK and
                                         FAULT_TENSORMAP apply to it.
                                         1 (default) = automatic: the thin kernel where it measured
