@@ -185,7 +185,7 @@ def test_thin_plans_of_other_grids_and_a_fresh_handle_on_freed_memory():
                     check(dD.cpu(), A, B, M, N, K, exact=True)
 
 
-@pytest.mark.parametrize("cluster", [0, 4])
+@pytest.mark.parametrize("cluster", [0, 2, 4])  # across the SMs; clusters that push, and that pull, partials
 def test_thin_watchdog_gives_up_and_the_handle_recovers(cluster):
     M, N, K = 16, 4096, 4096
     A, B = inputs.make_problem(M, N, K, "int2", seed=111)
