@@ -8,7 +8,7 @@
 // The ring is then up to 12 stages deep and keeps ~2x the bytes in flight per
 // SM.
 //
-// One CTA per SM, no clusters.  Roles:
+// At most one CTA per SM (shared memory), in clusters or not (below).  Roles:
 //   warp 0, lane 0   TMA producer: for each of the CTA's items, per k-block:
 //                    wait "empty", expect_tx, load the large tile (64 x 128)
 //                    and the small one (64 x NT)
@@ -16,10 +16,10 @@
 //                    of two NT-column tensor-memory accumulators, commit ->
 //                    "empty"; after an item, commit -> accumulator full
 //   warp 2           allocates (and frees) tensor memory
-//   warps 4-7        epilogue: tensor memory -> registers; whole tiles are
-//                    stored directly; of a split tile's pieces, the one holding
-//                    k-block 0 (the last item of its range) adds the others'
-//                    fp32 partials and stores the tile (thin_split.h)
+//   warps 4-7        epilogue: tensor memory -> registers; a split tile's
+//                    pieces meet as described below; the CTA's last tile is
+//                    staged in the drained ring and written by one TMA store
+//                    when D allows it, other tiles by the threads
 // Every wait is bounded by the watchdog (WaitCtl in ptx.cuh).
 //
 // Two ways to split the work.  Across the SMs (the default for large or long
@@ -31,21 +31,23 @@
 // arrives, per epilogue warp, on a barrier of rank 0 with release at cluster
 // scope; rank 0's warp waits on it (bounded), reads the rows of ranks 1..C-1
 // through distributed shared memory in rank order, adds, and stores.  Where
-// rank 0's shared memory has room for the others' partials beside a full ring,
-// they store them there instead (remote stores, which do not wait) and rank 0
-// reads its own shared memory.  A cluster barrier at exit keeps every rank's
-// shared memory alive until rank 0 has read it.  One CTA per whole tile is the cluster form with C = 1.
+// rank 0's shared memory has room for the others' partials beside a full
+// ring, they store them there instead (remote stores, which do not wait) and
+// rank 0 reads its own shared memory.  A cluster barrier at exit keeps every
+// rank's shared memory alive until rank 0 has read it.  One CTA per whole
+// tile is the cluster form with C = 1.
 //
-// Across the SMs, a split tile's pieces meet through fp32 partials in a
-// workspace and one flag per partial slot and epilogue warp.  A contributor warp stores its 32 rows,
-// meets at a warp barrier, and its lane 0 writes the launch's epoch to the
-// flag with a release store; the owner warp's lane 0 polls the flag with
-// acquire loads, the warp meets at a warp barrier, and the 32 lanes read the
-// rows.  The four warps of a CTA do not wait for one another on this path.
-// The epoch lives in device memory: every CTA reads it after the
-// grid-dependency wait, and the last CTA to have read it advances it for the
-// next launch, so launches replayed from a CUDA graph get a new epoch each
-// time as well, and flags never need clearing.
+// Across the SMs, the piece of a split tile that holds k-block 0 (the last
+// item of its range) owns the tile (thin_split.h), and the pieces meet through
+// fp32 partials in a workspace and one flag per partial slot and epilogue
+// warp.  A contributor warp stores its 32 rows, meets at a warp barrier, and
+// its lane 0 writes the launch's epoch to the flag with a release store; the
+// owner warp's lane 0 polls the flag with acquire loads, the warp meets at a
+// warp barrier, and the 32 lanes read the rows.  The four warps of a CTA do
+// not wait for one another on this path.  The epoch lives in device memory:
+// every CTA reads it after the grid-dependency wait, and the last CTA to have
+// read it advances it for the next launch, so launches replayed from a CUDA
+// graph get a new epoch each time as well, and flags never need clearing.
 #pragma once
 
 #include "gemm_kernels.h"
