@@ -31,11 +31,11 @@
 // arrives, per epilogue warp, on a barrier of rank 0 with release at cluster
 // scope; rank 0's warp waits on it (bounded), reads the rows of ranks 1..C-1
 // through distributed shared memory in rank order, adds, and stores.  Where
-// rank 0's shared memory has room for the others' partials beside a full
-// ring, they store them there instead (remote stores, which do not wait) and
-// rank 0 reads its own shared memory.  A cluster barrier at exit keeps every
-// rank's shared memory alive until rank 0 has read it.  One CTA per whole
-// tile is the cluster form with C = 1.
+// rank 0's shared memory has room for the others' partials beside a ring of
+// at least 4 stages, they store them there instead (remote stores, which do
+// not wait) and rank 0 reads its own shared memory.  A cluster barrier at exit
+// keeps every rank's shared memory alive until rank 0 has read it.  One CTA
+// per whole tile is the cluster form with C = 1.
 //
 // Across the SMs, the piece of a split tile that holds k-block 0 (the last
 // item of its range) owns the tile (thin_split.h), and the pieces meet through
