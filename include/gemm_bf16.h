@@ -286,10 +286,10 @@ GEMM_BF16_API int gemm_bf16_plan_info(gemm_bf16_t h, gemm_bf16_plan_info_t *info
 
 /* Enqueues D = A * B^T on `stream` and returns without synchronising.
  * Launches of one handle share its device scratch (stream-K workspace, tile
- * counter, thin-kernel partials and flags, packed operand copies): do not
- * let two launches of the same handle run at the same time (e.g. on two
- * streams without an ordering between them);
- * use one handle per stream instead.  When the plan repacks an operand
+ * counter, thin-kernel partials, flags and epoch, packed operand copies): do
+ * not let two launches of the same handle run at the same time (e.g. on two
+ * streams without an ordering between them); use one handle per stream
+ * instead.  When the plan repacks an operand
  * (plan_info.repack) a copy kernel runs on `stream` before the GEMM.
  *   A: device, M rows of lda bf16 (first K read);  B: device, N rows of ldb;
  *   D: device, M rows of ldd bf16 -- only the M x N sub-matrix is written.
